@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark: MLA paged decode, microseconds per layer-step, on GB300.
+
+A layer-step is one pass of the whole hot path over one batch: ``mla_decode`` on every
+emulated DCP shard (partial out + LSE per shard) and ``lse_merge`` of the partials.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config cp2] [--extra-configs tiny,plain,spec,long]
+
+The headline workload is ``cp2`` (8 requests, 64 heads, q_len 4, contexts U[1024, 8192],
+block_size 64, 2 shards, base-2 LSE).  Its 42 MB of KV fits in L2, so L2 is flushed
+(a 512 MB write) before every timed step; only the step itself is inside the CUDA-event
+bracket.  The other workloads are timed the same way and reported under
+``per_config``.  ``--impl reference`` times the float64 CPU oracle on the host cores.
+
+One JSON line is printed by rank 0.  With torchrun (N > 1) every rank runs an
+independent replica on its own GPU (weak scaling; the step has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+for _p in (ROOT, os.path.join(ROOT, "tests")):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MLA paged decode µs/layer-step, KV GB/s & TFLOP/s vs GB300 roofline"
+UNIT = "us/layer-step"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (per the decode definition; masked / padded work excluded)
+# ---------------------------------------------------------------------------
+def _row_prefixes(G, q_len):
+    G = np.asarray(G, dtype=np.int64)
+    return np.maximum(G[:, None] - np.arange(q_len - 1, -1, -1)[None, :], 0)
+
+
+def _local(Gr, cp, rank):
+    return Gr // cp + (Gr % cp > rank)
+
+
+def work(w):
+    """Algorithmic bytes and flops of one layer-step and of each shard's decode call."""
+    G = w.G.numpy()
+    Gr = _row_prefixes(G, w.q_len)
+    q_bytes = w.B * w.q_len * w.H * 576 * 2
+    per_shard = []
+    for r in range(w.cp):
+        L = np.minimum(_local(Gr, w.cp, r), _local(G, w.cp, r)[:, None])
+        Lfull = _local(G, w.cp, r)
+        per_shard.append(dict(flops=float((w.H * 2 * 1088 * L).sum()),
+                              bytes=float(Lfull.sum() * 1152 + q_bytes)))
+    return dict(kv_bytes=float(G.sum() * 1152), q_bytes=float(w.cp * q_bytes),
+                flops=float(sum(s["flops"] for s in per_shard)), per_shard=per_shard)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def time_config(name, steps, warmup, device, flush, with_e2e=False, event_calls=True):
+    import mla_paged_decode_03_gb300 as m
+    from mla_paged_decode_03_gb300.layer_step import DcpDecodeStep
+
+    w = synth.make_workload(name, device=device)
+    step = DcpDecodeStep.from_workload(w, device)
+    del w.kv_global
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(step.cp + 2)]
+          for _ in range(steps)]
+    step_ms, call_ms = [], []
+    torch.cuda.synchronize()
+    for k in range(steps):
+        flush.zero_()
+        e = ev[k]
+        e[0].record(stream)
+        if step.cp == 1:
+            step.run()
+            e[1].record(stream)
+        else:
+            for r in range(step.cp):
+                m.mla_decode(step.q, step.pools[r], step.block_table, step.seq_lens[r],
+                             step.gseq, step.q_len, step.cp, r, step.scale,
+                             out=step.partials[r], lse=step.lses[r], lse_base_e=step.lse_base_e,
+                             workspace=step.workspace)
+                e[r + 1].record(stream)
+            m.lse_merge(step.partials, step.lses, out=step.out, out_lse=step.out_lse,
+                        lse_base_e=step.lse_base_e)
+            e[step.cp + 1].record(stream)
+    torch.cuda.synchronize()
+    for k in range(steps):
+        e = ev[k]
+        last = e[1] if step.cp == 1 else e[step.cp + 1]
+        step_ms.append(e[0].elapsed_time(last))
+        for r in range(step.cp):
+            call_ms.append(e[r].elapsed_time(e[r + 1]))
+    assert m.device_status() == 0
+    wk = work(w)
+    res = dict(step_ms=step_ms, call_ms=call_ms, work=wk, w=w, step=step,
+               launches=step.kernel_launches_per_step())
+    if with_e2e:
+        res["e2e"] = time_e2e(step, steps, warmup, flush)
+    return res
+
+
+def time_e2e(step, steps, warmup, flush):
+    """Same step through the public API with host buffers: every step copies the
+    per-step inputs (q, block table, lengths) from pinned host memory and reads the
+    result (out, lse) back."""
+    dev = step.q.device
+    h_q = step.q.cpu().pin_memory()
+    h_bt = step.block_table.cpu().pin_memory()
+    h_sl = [s.cpu().pin_memory() for s in step.seq_lens]
+    h_g = step.gseq.cpu().pin_memory()
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h_lse = torch.empty(step.out_lse.shape, dtype=step.out_lse.dtype).pin_memory()
+    d_q = torch.empty_like(step.q)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        step.block_table.copy_(h_bt, non_blocking=True)
+        for s, hs in zip(step.seq_lens, h_sl):
+            s.copy_(hs, non_blocking=True)
+        step.gseq.copy_(h_g, non_blocking=True)
+        out, lse = step.run(q=d_q)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    h2d = (h_q.numel() * 2 + h_bt.numel() * 4 + sum(s.numel() * 4 for s in h_sl) +
+           h_g.numel() * 4)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    return dict(ms=statistics.mean(times), h2d=h2d, d2h=d2h)
+
+
+def summarize(res, pk):
+    wk = res["work"]
+    ms = statistics.mean(res["step_ms"])
+    t = ms * 1e-3
+    t_hbm = (wk["kv_bytes"] + wk["q_bytes"]) / (pk["hbm"] * 1e9)
+    t_tc = wk["flops"] / (pk["bf16"] * 1e12)
+    roof = max(t_hbm, t_tc)
+    call = statistics.mean(res["call_ms"]) * 1e-3
+    shard_flops = statistics.mean(s["flops"] for s in wk["per_shard"])
+    shard_bytes = statistics.mean(s["bytes"] for s in wk["per_shard"])
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    return dict(us_per_step=ms * 1e3, kv_gbs=wk["kv_bytes"] / t / 1e9,
+                tflops=wk["flops"] / t / 1e12, roofline_us=roof * 1e6,
+                roofline_frac=roof / t, bound=bound,
+                decode_call_us=call * 1e6,
+                decode_call_tflops=shard_flops / call / 1e12,
+                decode_call_gbs=shard_bytes / call / 1e9,
+                kv_gb=wk["kv_bytes"] / 1e9, gflop=wk["flops"] / 1e9,
+                launches_per_step=res["launches"])
+
+
+def cpu_baseline_sample(name, budget_s=12.0):
+    """Times the float64 oracle on the host cores on a bounded sample of the workload:
+    whole requests (all shards + merge) until ~budget_s of CPU work, scaled to one
+    layer-step by the share of the step's flops the sample covered."""
+    import oracle.mla_ref as R
+
+    w = synth.make_workload(name)
+    wk = work(w)
+    q = w.q.double().numpy()
+    bt = w.block_table.numpy()
+    G = w.G.numpy()
+    order = list(range(w.B))
+    done_flops, elapsed, used = 0.0, 0.0, []
+    Gr = _row_prefixes(G, w.q_len)
+    for b in order:
+        rows_b = w.rows_of(b).double().numpy()
+        t0 = time.perf_counter()
+        outs, lses = [], []
+        for r in range(w.cp):
+            o, l = R.ref_mla_decode_global(q[b:b + 1], [rows_b], G[b:b + 1], w.q_len, w.cp, r,
+                                           w.scale, w.base_e)
+            outs.append(o)
+            lses.append(l)
+        if w.cp > 1:
+            R.ref_lse_merge(np.stack(outs), np.stack(lses), w.base_e)
+        elapsed += time.perf_counter() - t0
+        done_flops += float((w.H * 2 * 1088 * Gr[b]).sum())
+        used.append(b)
+        if elapsed >= budget_s:
+            break
+    frac = done_flops / wk["flops"]
+    us = elapsed / frac * 1e6
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return dict(value=us, unit=UNIT, cores=threads, kind="oracle",
+                sample=f"{len(used)} of {w.B} requests of '{name}' (all {w.cp} shards + merge,"
+                       f" {frac * 100:.1f}% of the step's flops, {elapsed:.1f} s), scaled to one step")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import mla_paged_decode_03_gb300 as m
+    m._lib.load()
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    per_config = {}
+    extra = [c for c in args.extra_configs.split(",") if c and c != args.config]
+    for name in extra:
+        r = time_config(name, max(3, args.steps), max(3, args.warmup), device, flush)
+        per_config[name] = summarize(r, pk)
+        del r
+        torch.cuda.empty_cache()
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    wall0 = time.perf_counter()
+    res = time_config(args.config, args.steps, args.warmup, device, flush, with_e2e=True)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    s = summarize(res, pk)
+    per_config[args.config] = s
+    ms = reduce_max(s["us_per_step"] / 1e3, ws, device)
+    e2e_ms = reduce_max(res["e2e"]["ms"], ws, device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        return
+    peak_tc = pk["bf16"]
+    if s["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": s["decode_call_tflops"], "peak": peak_tc,
+                "unit": "TFLOP/s", "frac": s["decode_call_tflops"] / peak_tc}
+    else:
+        roof = {"bound": "hbm", "achieved": s["decode_call_gbs"], "peak": pk["hbm"],
+                "unit": "GB/s", "frac": s["decode_call_gbs"] / pk["hbm"]}
+    roof.update({"traffic": None, "kernel": "mla_decode call (split-KV decode + split combine)",
+                 "peak_source": pk["source"] + " (burst)"})
+    cpu = cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "B": res["w"].B, "H": res["w"].H,
+                   "q_len": res["w"].q_len, "block_size": res["w"].bs, "shards": res["w"].cp,
+                   "contexts": "U[1024,8192]" if args.config == "cp2" else "see synth",
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single GPU, emulated DCP shards"},
+        "kv_gbs": s["kv_gbs"], "tflops": s["tflops"], "roofline_frac": s["roofline_frac"],
+        "roofline_us": s["roofline_us"],
+        "roofline": roof,
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": res["e2e"]["h2d"],
+                "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "gpu_launches": res["launches"] * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "per_config": per_config,
+        "peaks": pk,
+        "wall_s": wall,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.config
+    budget = float(os.environ.get("REF_SAMPLE_SECONDS", min(8.0, 120.0 / max(1, args.steps))))
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline_sample(name, budget_s=0.5)
+    last = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        last = cpu_baseline_sample(name, budget_s=budget)
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    v = statistics.mean(vals)
+    last["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": name, "parallelism": "host cores (float64 CPU oracle)"},
+            "cpu_baseline": last,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="cp2", choices=synth.ORDER)
+    ap.add_argument("--extra-configs", default="tiny,plain,spec,long")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: paged multi-head-latent-attention (MLA)
+ * decode with decode-context-parallel (DCP) shards, the LSE merge of shard partials,
+ * and DCP slot mapping, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages summarising vLLM pull requests):
+ *   [#52188] "支持 Kimi-K3 DSpark 推测解码与 DCP 并行组合" (vLLM PR 52188)
+ *   [#54012] "带 DCP 的 MLA decode 改用 FlashInfer 原生 CP mask" (vLLM PR 54012)
+ *   [#48180] "为 TokenSpeed MLA 后端添加 DCP 与 Eagle 支持" (vLLM PR 48180)
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
+ *     The library allocates no memory and keeps no state between calls other than one
+ *     device status word per device (see mla_get_device_status).
+ *   - Every call is asynchronous on `stream` (the legacy default stream when NULL) and
+ *     returns one of the MLA_* codes.  Argument errors are found on the host before
+ *     anything is launched; mla_last_error() then returns a message (thread-local).
+ *   - bf16 means IEEE bfloat16 stored as 16-bit words; results are rounded to nearest
+ *     even.  Tensors are dense and row-major unless a stride is given.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without pulling in the CUDA headers. */
+typedef struct CUstream_st* mla_stream_t;
+
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad size, range or alignment    */
+#define MLA_ERR_UNSUPPORTED (-2)      /* valid request this build does not implement   */
+#define MLA_ERR_CUDA (-3)             /* a CUDA runtime call or kernel launch failed    */
+#define MLA_ERR_DEVICE (-4)           /* a kernel flagged bad data (see status word)    */
+
+#define MLA_PAD_SLOT_ID (-1)   /* slot of a position this rank does not own            */
+#define MLA_HEAD_DIM_QK 576    /* 512 latent (kv_lora_rank) + 64 rope dims            */
+#define MLA_HEAD_DIM_V 512     /* V is the first 512 dims of each latent KV row        */
+#define MLA_MAX_Q_LEN 16
+
+/* Bits of the device status word. */
+#define MLA_STATUS_BAD_PAGE 1u        /* block_table entry outside [0, num_blocks)      */
+#define MLA_STATUS_SEQ_TOO_LONG 2u    /* seq_lens[b] > max_blocks * block_size          */
+#define MLA_STATUS_BAD_VBLOCK 4u      /* cp_local_slot: virtual block >= max_blocks     */
+#define MLA_STATUS_WAIT_TIMEOUT 8u    /* a bounded on-chip wait gave up                 */
+
+/*
+ * Bytes of workspace that mla_decode uses to split one request's KV range over several
+ * thread blocks (split-KV) for a batch of B requests, H query heads, q_len query rows
+ * and a device with num_sms SMs.  Passing less (or NULL) is allowed: the call then uses
+ * fewer splits, down to none.  Pure function of its arguments; no CUDA call.
+ */
+size_t mla_decode_workspace_size(int B, int H, int q_len, int num_sms);
+
+/*
+ * mla_decode -- one shard's partial attention for a batch of multi-token decode blocks.
+ *
+ * Defines ([#54012] "关键源码片段", the native-DCP call; [#52188] "关键源码片段",
+ * _prepare_flattened_decode_metadata; [#48180] "实现拆解" step 1):
+ *   query row i (0 <= i < q_len) of request b sees the global prefix
+ *       G_i = max(0, causal_seqlens_global[b] - (q_len - 1 - i)),
+ *   this shard (round-robin interleave 1: global position g lives on rank g % cp_world
+ *   at local position g / cp_world) holds
+ *       L_i = min(seq_lens[b], G_i / cp_world + (G_i % cp_world > cp_rank)),
+ *   and the local key l < L_i is row  kv_cache[block_table[b*bt_stride + l/block_size]]
+ *   [l % block_size].  With s_l = scale * <q_row, key_l> over all 576 dims,
+ *       out = sum_l softmax(s)_l * key_l[0:512],   lse = log(sum_l exp(s_l)),
+ *   lse in natural log when lse_base_e != 0, else in log2.  A row with L_i = 0 gets
+ *   out = 0 and lse = -inf.
+ *
+ * Arguments:
+ *   q            bf16 [B, q_len, H, 576], 16-byte aligned.
+ *   kv_cache     bf16 [num_blocks, block_size, 576] (this shard's pool), 16-byte aligned.
+ *   block_table  int32 [B, bt_stride]; only the first ceil(L/block_size) entries of a
+ *                row are read.  An entry outside [0, num_blocks) is not dereferenced:
+ *                its keys are read as zeros and MLA_STATUS_BAD_PAGE is set.
+ *   seq_lens     int32 [B], this shard's token count of each request.  A value above
+ *                max_blocks*block_size is clamped and MLA_STATUS_SEQ_TOO_LONG is set.
+ *   causal_seqlens_global  int32 [B] global lengths; may be NULL only if cp_world == 1,
+ *                then seq_lens is used.
+ *   B >= 0, 1 <= H, 1 <= q_len <= MLA_MAX_Q_LEN, block_size >= 1, num_blocks >= 1,
+ *   1 <= max_blocks <= bt_stride, 1 <= cp_world, 0 <= cp_rank < cp_world, finite scale.
+ *   out          bf16 [B*q_len, H, 512], 16-byte aligned.
+ *   lse          float [B*q_len, H] or NULL.
+ *   workspace    device scratch of workspace_bytes (may be NULL / 0), 256-byte aligned.
+ * Errors: MLA_ERR_INVALID_ARGUMENT for any violated condition above (nothing launched),
+ *   MLA_ERR_CUDA if a launch fails.
+ */
+int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+               int64_t bt_stride, const int32_t* seq_lens,
+               const int32_t* causal_seqlens_global, int B, int H, int q_len,
+               int block_size, int num_blocks, int max_blocks, int cp_world, int cp_rank,
+               float scale, void* out, float* lse, int lse_base_e, void* workspace,
+               size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * lse_merge -- combine n_shards partial results of the same rows through their LSEs.
+ *
+ * Defines ([#54012] "实现拆解" step 3: shards are merged across ranks and must agree on
+ * the LSE base; [#48180] "实现拆解" step 2: merge when DCP is on): per row (t, h),
+ *   M = max_s lses[s,t,h],  w_s = base^(lses[s,t,h] - M),
+ *   out[t,h,:] = sum_s w_s partials[s,t,h,:] / sum_s w_s,
+ *   out_lse[t,h] = M + log_base(sum_s w_s),
+ * base e when lse_base_e != 0, else 2.  A shard with lse = -inf has weight 0 and its
+ * partial is not read; if every shard has -inf, out = 0 and out_lse = -inf.
+ *
+ * Arguments:
+ *   partials        [n_shards, T, H, 512], bf16 when partials_fp32 == 0 else float,
+ *                   16-byte aligned.
+ *   lses            float [n_shards, T, H].
+ *   n_shards >= 1, T >= 0, H >= 1.
+ *   out             bf16 [T, H, 512], 16-byte aligned.
+ *   out_lse         float [T, H] or NULL.
+ * Errors: MLA_ERR_INVALID_ARGUMENT, MLA_ERR_CUDA.
+ */
+int lse_merge(const void* partials, int partials_fp32, const float* lses, int n_shards,
+              int T, int H, void* out, float* out_lse, int lse_base_e,
+              mla_stream_t stream);
+
+/*
+ * cp_local_slot -- this rank's KV slot of each position, MLA_PAD_SLOT_ID otherwise.
+ *
+ * Defines ([#52188] "关键源码片段", cp_utils.py cp_local_slot; "实现拆解" step 4): a
+ * virtual block spans block_size*cp_size global positions and block_table[b, pos /
+ * (block_size*cp_size)] names its page on every rank; with o = pos % (block_size*cp_size),
+ * position pos is owned by rank (o / interleave) % cp_size, at local offset
+ * (o / (interleave*cp_size)) * interleave + o % interleave, so
+ *     slots[b,n] = page * block_size + local offset   if this rank owns it,
+ *     slots[b,n] = MLA_PAD_SLOT_ID                     otherwise, or when pos < 0
+ * (a negative position marks a rejected draft position).  cp_size == 1 gives
+ * page * block_size + pos % block_size.
+ *
+ * Arguments:
+ *   positions    int64 [B, N];  block_table int32 [B, bt_stride] with max_blocks valid
+ *                columns;  slots int64 [B, N].
+ *   B >= 0, N >= 0, block_size >= 1, cp_size >= 1, 0 <= cp_rank < cp_size,
+ *   interleave >= 1 with block_size % interleave == 0, 1 <= max_blocks <= bt_stride.
+ * A position whose virtual block is >= max_blocks gets MLA_PAD_SLOT_ID and sets
+ * MLA_STATUS_BAD_VBLOCK; its table entry is not read.
+ * Errors: MLA_ERR_INVALID_ARGUMENT, MLA_ERR_CUDA.
+ */
+int cp_local_slot(const int64_t* positions, const int32_t* block_table, int64_t bt_stride,
+                  int max_blocks, int B, int N, int block_size, int cp_size, int cp_rank,
+                  int interleave, int64_t* slots, mla_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's status word.
+ * Returns MLA_OK when no kernel flagged anything since the last call, MLA_ERR_DEVICE
+ * when one did (mla_last_error() names the bits; *bits_out receives them if non-NULL),
+ * MLA_ERR_CUDA if the read itself failed.
+ */
+int mla_get_device_status(mla_stream_t stream, uint32_t* bits_out);
+
+/* Message of the calling thread's last failed call (empty string if none). */
+const char* mla_last_error(void);
+
+/* ABI version of this library: (major << 16) | minor. */
+int mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,227 @@
+// C ABI of libmla_decode.so (declared in include/mla_decode.h): host-side argument
+// validation, error reporting and kernel launches.  Nothing here allocates memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "../../include/mla_decode.h"
+
+namespace {
+
+// One status word per device; kernels OR MLA_STATUS_* bits into it.
+__device__ unsigned int g_mla_status = 0;
+
+thread_local char t_err[512] = {0};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  t_err[0] = 0;
+  return MLA_OK;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready;
+  int num_sms;
+  unsigned int* status;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Resolves the current device's SM count and status-word address (once per device).
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device index %d", dev);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mla_status);
+    if (e != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    d.num_sms = sms;
+    d.status = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MLA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int mla_abi_version(void) { return (1 << 16) | 0; }
+
+const char* mla_last_error(void) { return t_err; }
+
+size_t mla_decode_workspace_size(int B, int H, int q_len, int num_sms) {
+  if (B <= 0 || H <= 0 || q_len <= 0 || num_sms <= 0) return 0;
+  return mla::decode_workspace_size(B, H, q_len, num_sms);
+}
+
+int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+               int64_t bt_stride, const int32_t* seq_lens,
+               const int32_t* causal_seqlens_global, int B, int H, int q_len,
+               int block_size, int num_blocks, int max_blocks, int cp_world, int cp_rank,
+               float scale, void* out, float* lse, int lse_base_e, void* workspace,
+               size_t workspace_bytes, mla_stream_t stream) {
+  if (B < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: B=%d < 0", B);
+  if (H < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: H=%d < 1", H);
+  if (q_len < 1 || q_len > MLA_MAX_Q_LEN)
+    return fail(q_len < 1 ? MLA_ERR_INVALID_ARGUMENT : MLA_ERR_UNSUPPORTED,
+                "mla_decode: q_len=%d outside [1, %d]", q_len, MLA_MAX_Q_LEN);
+  if (block_size < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: block_size < 1");
+  if (num_blocks < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: num_blocks < 1");
+  if (max_blocks < 1 || bt_stride < max_blocks)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: need 1 <= max_blocks (%d) <= bt_stride (%lld)",
+                max_blocks, (long long)bt_stride);
+  if ((long long)max_blocks * block_size > (1LL << 31) - 1)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: max_blocks*block_size exceeds 2^31-1");
+  if ((long long)num_blocks * block_size > (1LL << 40))
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: cache too large");
+  if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: need 0 <= cp_rank (%d) < cp_world (%d)",
+                cp_rank, cp_world);
+  if (!isfinite(scale)) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: scale not finite");
+  if (B == 0) return ok();
+  if (!q || !kv_cache || !block_table || !seq_lens || !out)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: null q/kv_cache/block_table/seq_lens/out");
+  if (causal_seqlens_global == nullptr && cp_world != 1)
+    return fail(MLA_ERR_INVALID_ARGUMENT,
+                "mla_decode: causal_seqlens_global is required when cp_world > 1");
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: q, kv_cache and out must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      (causal_seqlens_global && !aligned(causal_seqlens_global, 4)) || (lse && !aligned(lse, 4)))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: misaligned int32/float argument");
+  if (workspace && !aligned(workspace, 256))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: workspace must be 256-byte aligned");
+  if ((long long)B * q_len * H > (1LL << 31) - 1)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: too many query rows");
+
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != MLA_OK) return rc;
+
+  mla::DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint16_t*>(kv_cache);
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.gseq = causal_seqlens_global ? causal_seqlens_global : seq_lens;
+  a.B = B;
+  a.H = H;
+  a.q_len = q_len;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks;
+  a.cp_world = cp_world;
+  a.cp_rank = cp_rank;
+  a.scale = scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.lse_base_e = lse_base_e ? 1 : 0;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace ? workspace_bytes : 0;
+  a.num_sms = dev->num_sms;
+  a.status = dev->status;
+  cudaError_t e = mla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "mla_decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int lse_merge(const void* partials, int partials_fp32, const float* lses, int n_shards,
+              int T, int H, void* out, float* out_lse, int lse_base_e, mla_stream_t stream) {
+  if (n_shards < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "lse_merge: n_shards=%d < 1", n_shards);
+  if (T < 0 || H < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "lse_merge: need T >= 0, H >= 1");
+  if (T == 0) return ok();
+  if (!partials || !lses || !out)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "lse_merge: null partials/lses/out");
+  if (!aligned(partials, 16) || !aligned(out, 16) || !aligned(lses, 4) ||
+      (out_lse && !aligned(out_lse, 4)))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "lse_merge: partials/out need 16-byte alignment");
+  const long long rows = (long long)T * H;
+  cudaError_t e = mla::launch_lse_combine(partials, partials_fp32 != 0, lses, n_shards, rows,
+                                          rows, !lse_base_e, lse_base_e ? 0.6931471805599453f : 1.f,
+                                          static_cast<uint16_t*>(out), out_lse,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "lse_merge launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int cp_local_slot(const int64_t* positions, const int32_t* block_table, int64_t bt_stride,
+                  int max_blocks, int B, int N, int block_size, int cp_size, int cp_rank,
+                  int interleave, int64_t* slots, mla_stream_t stream) {
+  if (B < 0 || N < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: B, N must be >= 0");
+  if (block_size < 1 || cp_size < 1 || interleave < 1)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: block_size, cp_size, interleave >= 1");
+  if (cp_rank < 0 || cp_rank >= cp_size)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: need 0 <= cp_rank < cp_size");
+  if (block_size % interleave != 0)
+    return fail(MLA_ERR_INVALID_ARGUMENT,
+                "cp_local_slot: block_size (%d) must be a multiple of interleave (%d)", block_size,
+                interleave);
+  if (max_blocks < 1 || bt_stride < max_blocks)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: need 1 <= max_blocks <= bt_stride");
+  if ((long long)B * N == 0) return ok();
+  if (!positions || !block_table || !slots)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: null positions/block_table/slots");
+  if (!aligned(positions, 8) || !aligned(slots, 8) || !aligned(block_table, 4))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "cp_local_slot: misaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != MLA_OK) return rc;
+  cudaError_t e = mla::launch_cp_local_slot(positions, block_table, bt_stride, max_blocks, B, N,
+                                            block_size, cp_size, cp_rank, interleave, slots,
+                                            dev->status, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "cp_local_slot launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int mla_get_device_status(mla_stream_t stream, uint32_t* bits_out) {
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "mla_get_device_status: %s", cudaGetErrorString(e));
+  unsigned int bits = 0;
+  e = cudaMemcpyFromSymbol(&bits, g_mla_status, sizeof(bits));
+  if (e == cudaSuccess) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_mla_status, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "mla_get_device_status: %s", cudaGetErrorString(e));
+  if (bits_out) *bits_out = bits;
+  if (bits == 0) return ok();
+  return fail(MLA_ERR_DEVICE, "device status 0x%x:%s%s%s%s", bits,
+              (bits & MLA_STATUS_BAD_PAGE) ? " bad block_table entry;" : "",
+              (bits & MLA_STATUS_SEQ_TOO_LONG) ? " seq_len beyond max_blocks*block_size;" : "",
+              (bits & MLA_STATUS_BAD_VBLOCK) ? " virtual block beyond max_blocks;" : "",
+              (bits & MLA_STATUS_WAIT_TIMEOUT) ? " on-chip wait timed out;" : "");
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal launcher interface shared by the translation units of libmla_decode.so.
+// Not part of the public ABI (include/mla_decode.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Arguments of one mla_decode call after host validation.
+struct DecodeArgs {
+  const uint16_t* q;             // bf16 [B*q_len*H, 576]
+  const uint16_t* kv;            // bf16 [num_blocks*block_size, 576]
+  const int32_t* block_table;    // [B, bt_stride]
+  int64_t bt_stride;
+  const int32_t* seq_lens;       // [B]
+  const int32_t* gseq;           // [B] global lengths (seq_lens when cp_world == 1)
+  int B, H, q_len, block_size, num_blocks, max_blocks, cp_world, cp_rank;
+  float scale;
+  uint16_t* out;                 // bf16 [B*q_len*H, 512]
+  float* lse;                    // [B*q_len*H] or null
+  int lse_base_e;
+  void* workspace;
+  size_t workspace_bytes;
+  int num_sms;
+  unsigned int* status;          // device status word
+};
+
+// Split-KV decode: returns cudaError_t of the launches.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+size_t decode_workspace_size(int B, int H, int q_len, int num_sms);
+
+// LSE combine of n partials per row.  in_log2: lses are base-2 (else base e).
+// out_lse_mul: multiplier applied to the base-2 merged LSE before it is stored
+// (1 for base 2, ln 2 for base e).  partial_row_stride: elements between rows of one
+// shard (512 for dense), shard_stride: elements between shards.
+cudaError_t launch_lse_combine(const void* partials, bool partials_fp32, const float* lses,
+                               int n, long long rows, long long shard_stride_rows,
+                               bool in_log2, float out_lse_mul, uint16_t* out,
+                               float* out_lse, cudaStream_t stream);
+
+cudaError_t launch_cp_local_slot(const int64_t* positions, const int32_t* block_table,
+                                 int64_t bt_stride, int max_blocks, int B, int N,
+                                 int block_size, int cp_size, int cp_rank, int interleave,
+                                 int64_t* slots, unsigned int* status, cudaStream_t stream);
+
+}  // namespace mla

@@ -183,6 +183,25 @@ def make_workload(name: str, device: str = "cpu", lengths: Optional[List[int]] =
                     block_table=bt, num_blocks=num_blocks, slot_cases=slot_cases)
 
 
+def make_custom(B: int, H: int, q_len: int, lengths, bs: int, cp: int, base_e: bool = True,
+                seed: int = 0, outlier_frac: float = 0.0, device: str = "cpu",
+                spare_columns: int = 1) -> Workload:
+    """An ad-hoc workload with the same drawing rules (edge-case tests)."""
+    name = f"custom_{seed}"
+    CONFIGS[name] = dict(B=B, H=H, q_len=q_len, ctx=tuple(lengths), bs=bs, cp=cp,
+                         base_e=base_e, seed=seed, outlier_frac=outlier_frac)
+    try:
+        w = make_workload(name, device=device, lengths=list(lengths))
+    finally:
+        del CONFIGS[name]
+    if spare_columns != 1:
+        bt = w.block_table
+        extra = torch.full((bt.shape[0], spare_columns), w.num_blocks - 1, dtype=torch.int32)
+        w.block_table = torch.cat([bt[:, :-1], extra], 1) if spare_columns > 0 else bt[:, :-1]
+    w.name = name
+    return w
+
+
 def poisoned_pool(num_blocks: int, bs: int, device: str = "cpu") -> torch.Tensor:
     """A shard pool [num_blocks, bs, 576] bf16 filled with NaN; every slot that a
     request does not own stays NaN, so any read outside the visible set shows up."""

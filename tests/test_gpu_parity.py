@@ -1,0 +1,260 @@
+"""CUDA path (through the C ABI) against the float64 oracle, element by element.
+
+Slot mapping must be bit-exact; decode outputs and merged outputs must be within the
+tolerances stated in gpu_helpers.  Pools are filled with NaN wherever no KV row lives,
+so a read of an unreferenced page or of a slot past a request's length shows up as a
+non-finite output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_decode_03_gb300 as M
+import oracle.mla_ref as R
+import synth
+from mla_paged_decode_03_gb300.dcp import build_shard_pool, local_seq_lens
+from mla_paged_decode_03_gb300.layer_step import DcpDecodeStep
+
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _clean_status():
+    M.device_status()
+    yield
+
+
+# ---------------------------------------------------------------------------
+# cp_local_slot
+# ---------------------------------------------------------------------------
+def _slot_case_check(case):
+    pos = case.positions
+    bt = case.block_table
+    for rank in range(case.cp_size):
+        want = R.ref_cp_local_slot(pos.numpy(), bt.numpy(), case.block_size, case.cp_size, rank,
+                                   case.interleave)
+        got = M.cp_local_slot(pos.to(DEV), bt.to(DEV), case.block_size, case.cp_size, rank,
+                              case.interleave).cpu().numpy()
+        assert np.array_equal(got, want), (rank, np.argwhere(got != want)[:5])
+    assert M.device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "cp2", "long"])
+def test_cp_local_slot_workloads(name):
+    w = synth.make_workload(name)
+    assert w.slot_cases
+    for case in w.slot_cases:
+        if case.positions.numel() > 300000:
+            # the oracle's per-position loop is slow: check a strided sample of rows'
+            # positions bit-exactly, and the whole output against the PAD pattern rules
+            _slot_large_check(case)
+        else:
+            _slot_case_check(case)
+
+
+def _slot_large_check(case):
+    pos, bt = case.positions, case.block_table
+    for rank in range(case.cp_size):
+        got = M.cp_local_slot(pos.to(DEV), bt.to(DEV), case.block_size, case.cp_size, rank,
+                              case.interleave).cpu().numpy()
+        idx = np.arange(0, pos.shape[1], 97)
+        want = R.ref_cp_local_slot(pos.numpy()[:, idx], bt.numpy(), case.block_size,
+                                   case.cp_size, rank, case.interleave)
+        assert np.array_equal(got[:, idx], want)
+        tail = slice(pos.shape[1] - 4096, pos.shape[1])
+        want_t = R.ref_cp_local_slot(pos.numpy()[:, tail], bt.numpy(), case.block_size,
+                                     case.cp_size, rank, case.interleave)
+        assert np.array_equal(got[:, tail], want_t)
+        owner = (pos.numpy() // case.interleave) % case.cp_size
+        assert np.array_equal(got >= 0, (owner == rank) & (pos.numpy() >= 0))
+    assert M.device_status() == 0
+
+
+@pytest.mark.parametrize("bs,cp,il,N", [(16, 2, 1, 167), (64, 8, 1, 1000), (16, 4, 2, 333),
+                                        (64, 16, 4, 2048), (32, 1, 1, 99), (8, 3, 2, 50),
+                                        (64, 2, 64, 640)])
+def test_cp_local_slot_shapes(bs, cp, il, N):
+    g = torch.Generator().manual_seed(bs * 1000 + cp * 10 + il)
+    B = 3
+    vb = (N + bs * cp - 1) // (bs * cp) + 1
+    bt = torch.randperm(B * vb * 3, generator=g)[:B * vb].to(torch.int32).reshape(B, vb)
+    pos = torch.randint(-3, N, (B, N), generator=g, dtype=torch.int64)
+    _slot_case_check(synth.SlotCase(pos, bt, bs, cp, il))
+
+
+def test_cp_local_slot_padded_table_stride():
+    bs, cp = 16, 2
+    bt_full = torch.randperm(64, generator=torch.Generator().manual_seed(1))[:24].to(
+        torch.int32).reshape(2, 12)
+    bt = bt_full[:, :5]                                  # row stride 12, 5 valid columns
+    pos = torch.arange(0, 160, dtype=torch.int64).repeat(2, 1)
+    for rank in range(cp):
+        want = R.ref_cp_local_slot(pos.numpy(), bt.numpy(), bs, cp, rank, 1)
+        got = M.cp_local_slot(pos.to(DEV), bt_full.to(DEV)[:, :5], bs, cp, rank).cpu().numpy()
+        assert np.array_equal(got, want)
+
+
+def test_cp_local_slot_out_of_table_flags_status():
+    bt = torch.tensor([[3, 5]], dtype=torch.int32, device=DEV)
+    pos = torch.tensor([[0, 1, 63, 64, 65, 1000, -2]], dtype=torch.int64, device=DEV)
+    got = M.cp_local_slot(pos, bt, 16, 2, 0).cpu().numpy()[0]
+    assert list(got[3:]) == [-1, -1, -1, -1]              # virtual block 2+ is past the table
+    assert list(got[:3]) == [48, -1, 5 * 16 + 15]
+    assert M.device_status() & 4
+
+
+# ---------------------------------------------------------------------------
+# lse_merge
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n,fp32,base_e", [(1, False, True), (2, False, False), (8, False, True),
+                                           (16, True, True), (3, True, False), (40, False, True)])
+def test_lse_merge_parity(n, fp32, base_e):
+    g = torch.Generator().manual_seed(n * 7 + fp32)
+    T, Hh = 13, 24
+    parts = torch.randn(n, T, Hh, 512, generator=g)
+    parts = parts.to(torch.float32 if fp32 else torch.bfloat16)
+    lses = torch.randn(n, T, Hh, generator=g) * 5 + 10
+    empty = torch.rand(n, T, Hh, generator=g) < 0.3
+    lses[empty] = float("-inf")
+    lses[:, 0, 0] = float("-inf")                         # a row with no shard at all
+    wo, wl = R.ref_lse_merge(H.f64(parts), H.f64(lses), base_e)
+    out, ol = M.lse_merge(parts.to(DEV), lses.to(DEV), out_lse=torch.empty(T, Hh, device=DEV),
+                          lse_base_e=base_e)
+    H.compare(out, ol, wo, wl, what=f"merge n={n}")
+    assert torch.all(out[0, 0] == 0)
+
+
+def test_lse_merge_skips_nan_partials_of_empty_shards():
+    parts = torch.randn(2, 4, 8, 512).to(torch.bfloat16)
+    parts[1] = float("nan")
+    lses = torch.randn(2, 4, 8)
+    lses[1] = float("-inf")
+    out, _ = M.lse_merge(parts.to(DEV), lses.to(DEV))
+    assert torch.allclose(out.float().cpu(), parts[0].float(), atol=0, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# mla_decode: whole workloads at sizes the oracle finishes in seconds
+# ---------------------------------------------------------------------------
+def _gpu_shards(w, with_workspace=True):
+    step = DcpDecodeStep.from_workload(w, DEV)
+    if not with_workspace:
+        step.workspace = torch.empty(0, dtype=torch.uint8, device=DEV)
+    return step
+
+
+def _check_workload(w, relative=False, with_workspace=True):
+    step = _gpu_shards(w, with_workspace)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    ro, rl, mo, ml = H.oracle_shards(w)
+    if w.cp > 1:
+        for r in range(w.cp):
+            H.compare(step.partials[r], step.lses[r], ro[r], rl[r], relative, f"{w.name} shard {r}")
+    H.compare(out, lse, mo, ml, relative, f"{w.name} merged")
+    assert M.device_status() == 0
+
+
+def test_decode_tiny_full():
+    _check_workload(synth.make_workload("tiny"))
+
+
+def test_decode_cp2_full():
+    _check_workload(synth.make_workload("cp2"))
+
+
+@pytest.mark.parametrize("name,lengths", [
+    ("plain", [1000, 777, 2049]),
+    ("spec", [3000, 1234]),
+    ("long", [5000, 4097]),
+])
+def test_decode_reduced_workloads(name, lengths):
+    _check_workload(synth.make_workload(name, lengths=lengths), relative=(name == "long"))
+
+
+def test_decode_without_workspace_matches():
+    _check_workload(synth.make_workload("plain", lengths=[1500, 3000]), with_workspace=False)
+
+
+@pytest.mark.parametrize("q_len,lengths,cp", [
+    (1, [1, 2, 3], 1), (2, [1, 2], 1), (3, [1, 2, 3, 4], 2), (4, [1, 3, 5, 9], 4),
+    (4, [2, 17, 33], 16), (2, [15, 16, 17], 1), (3, [63, 64, 65, 127, 128, 129], 1),
+    (1, [191, 192, 193], 3), (8, [40, 300], 2),
+])
+@pytest.mark.parametrize("H_,bs", [(16, 16), (64, 64), (128, 64)])
+def test_decode_edge_cases(q_len, lengths, cp, H_, bs):
+    w = synth.make_custom(len(lengths), H_, q_len, lengths, bs, cp, base_e=(cp != 4),
+                          seed=q_len * 100 + cp + H_)
+    _check_workload(w)
+
+
+def test_decode_block_table_with_wide_stride():
+    w = synth.make_custom(2, 64, 2, [300, 129], 64, 2, seed=5, spare_columns=9)
+    _check_workload(w)
+
+
+def test_decode_bad_page_is_flagged_not_read():
+    w = synth.make_custom(2, 16, 1, [40, 40], 16, 1, seed=9)
+    step = _gpu_shards(w)
+    bt = step.block_table.clone()
+    bt[1, 1] = w.num_blocks + 1000                      # request 1, keys 16..31
+    step.block_table = bt
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    assert M.device_status() & 1
+    _, _, mo, ml = H.oracle_shards(w)
+    H.compare(out[:1], lse[:1], mo[:1], ml[:1], what="untouched request")
+    assert torch.isfinite(out[1].float()).all()
+
+
+def test_decode_seq_len_beyond_table_is_flagged():
+    w = synth.make_custom(1, 16, 1, [40], 16, 1, seed=10)
+    step = _gpu_shards(w)
+    step.seq_lens[0] = torch.tensor([10_000], dtype=torch.int32, device=DEV)
+    step.gseq = torch.tensor([10_000], dtype=torch.int32, device=DEV)
+    step.run()
+    torch.cuda.synchronize()
+    assert M.device_status() & 2                        # clamped, flagged, no fault
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration bench.py times, sampled rows
+# ---------------------------------------------------------------------------
+def _sampled_full(name, sample, relative=False):
+    w = synth.make_workload(name, device=DEV)
+    step = DcpDecodeStep.from_workload(w, DEV)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    assert M.device_status() == 0
+    get = H.device_row_getter(w)
+    outs, lses = [], []
+    for r in range(w.cp):
+        o, l = H.oracle_sampled_shard(w, sample, r, get)
+        outs.append(o)
+        lses.append(l)
+        if r < 2 and w.cp > 1:
+            idx = [b * w.q_len + i for b, i in sample]
+            H.compare(step.partials[r][idx], step.lses[r][idx], o[idx], l[idx], relative,
+                      f"{name} shard {r}")
+    mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), w.base_e)
+    idx = [b * w.q_len + i for b, i in sample]
+    H.compare(out[idx], lse[idx], mo[idx], ml[idx], relative, f"{name} merged")
+    # properties that hold for every row: finite outputs, |out| bounded by max |V|
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
+
+
+def test_full_size_plain_sampled():
+    _sampled_full("plain", [(0, 0), (17, 0), (63, 0)])
+
+
+def test_full_size_spec_sampled():
+    _sampled_full("spec", [(0, 0), (0, 3), (31, 1)])
+
+
+def test_full_size_long_sampled():
+    _sampled_full("long", [(2, 0), (2, 1)], relative=True)
