@@ -155,6 +155,16 @@ int cp_local_slot(const int64_t* positions, const int32_t* block_table, int64_t 
  */
 int mla_get_device_status(mla_stream_t stream, uint32_t* bits_out);
 
+/*
+ * Selects the decode kernel for later mla_decode calls in this process (diagnostics and
+ * tests): 0 = automatic (the tcgen05/TMEM/TMA kernel whenever block_size is 16, 32, 64 or
+ * 128, else the warp-level mma.sync kernel), 1 = always the warp-level kernel, 2 = the
+ * tcgen05 kernel where it applies.  Returns the previous choice, or
+ * MLA_ERR_INVALID_ARGUMENT for any other value.  Not thread-safe against concurrent
+ * mla_decode calls.
+ */
+int mla_set_decode_kernel(int choice);
+
 /* Message of the calling thread's last failed call (empty string if none). */
 const char* mla_last_error(void);
 

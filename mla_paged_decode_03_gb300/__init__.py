@@ -163,6 +163,18 @@ def cp_local_slot(positions: torch.Tensor, block_table: torch.Tensor, block_size
     return slots
 
 
+KERNEL_AUTO, KERNEL_MMA, KERNEL_TC = 0, 1, 2
+
+
+def set_decode_kernel(choice: int) -> int:
+    """0 = automatic, 1 = warp-level mma.sync kernel, 2 = tcgen05 kernel where it applies.
+    Returns the previous choice."""
+    rc = _lib.load().mla_set_decode_kernel(int(choice))
+    if rc < 0:
+        _lib.check(rc)
+    return rc
+
+
 def device_status(stream=None) -> int:
     """Waits for the stream, returns and clears the device status bits (0 = clean)."""
     bits = ctypes.c_uint32(0)

@@ -20,7 +20,8 @@ MLA_ERR_DEVICE = -4
 PAD_SLOT_ID = -1
 
 EXPORTED = ("mla_decode_workspace_size", "mla_decode", "lse_merge", "cp_local_slot",
-            "mla_get_device_status", "mla_last_error", "mla_abi_version")
+            "mla_get_device_status", "mla_set_decode_kernel", "mla_last_error",
+            "mla_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def load() -> ctypes.CDLL:
         lib.mla_get_device_status.argtypes = [c_vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.mla_last_error.restype = ctypes.c_char_p
         lib.mla_last_error.argtypes = []
+        lib.mla_set_decode_kernel.restype = c_int
+        lib.mla_set_decode_kernel.argtypes = [c_int]
         lib.mla_abi_version.restype = c_int
         lib.mla_abi_version.argtypes = []
         _lib = lib

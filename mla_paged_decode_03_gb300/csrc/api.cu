@@ -71,6 +71,16 @@ extern "C" {
 
 int mla_abi_version(void) { return (1 << 16) | 0; }
 
+int mla_set_decode_kernel(int choice) {
+  static int current = 0;
+  if (choice < 0 || choice > 2)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_set_decode_kernel: choice %d not in 0..2", choice);
+  const int prev = current;
+  current = choice;
+  mla::set_decode_kernel_choice(choice);
+  return prev;
+}
+
 const char* mla_last_error(void) { return t_err; }
 
 size_t mla_decode_workspace_size(int B, int H, int q_len, int num_sms) {

@@ -1,0 +1,25 @@
+// Kernel choice for mla_decode: the tcgen05 kernel wherever the KV layout allows TMA
+// tiles, the warp-level kernel otherwise.
+#include "internal.h"
+
+namespace mla {
+namespace {
+int g_choice = 0;
+}
+
+void set_decode_kernel_choice(int choice) { g_choice = choice; }
+
+size_t decode_workspace_size(int B, int H, int q_len, int num_sms) {
+  const size_t a = tc_workspace_size(B, H, q_len, num_sms);
+  const size_t b = mma_workspace_size(B, H, q_len, num_sms);
+  return a > b ? a : b;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.B == 0 || a.H * a.q_len == 0) return cudaSuccess;
+  const bool tc = g_choice == 2 || (g_choice == 0 && tc_supported(a));
+  if (tc && tc_supported(a)) return launch_decode_tc(a, stream);
+  return launch_decode_mma(a, stream);
+}
+
+}  // namespace mla

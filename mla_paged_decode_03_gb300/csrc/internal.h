@@ -27,9 +27,22 @@ struct DecodeArgs {
   unsigned int* status;          // device status word
 };
 
-// Split-KV decode: returns cudaError_t of the launches.
+// Split-KV decode: picks the tensor-core (tcgen05) kernel when the cache layout allows
+// TMA tiles (block_size 16/32/64/128), else the warp-level MMA kernel.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 size_t decode_workspace_size(int B, int H, int q_len, int num_sms);
+
+// tcgen05 / TMEM / TMA kernel (mla_decode_tc.cu)
+bool tc_supported(const DecodeArgs& a);
+size_t tc_workspace_size(int B, int H, int q_len, int num_sms);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+
+// warp-level mma.sync kernel (mla_decode_mma.cu)
+size_t mma_workspace_size(int B, int H, int q_len, int num_sms);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
+
+// Testing hook: 0 = automatic choice, 1 = force the warp-level kernel, 2 = force tcgen05.
+void set_decode_kernel_choice(int choice);
 
 // LSE combine of n partials per row.  in_log2: lses are base-2 (else base e).
 // out_lse_mul: multiplier applied to the base-2 merged LSE before it is stored

@@ -347,11 +347,11 @@ size_t ws_bytes_for(int B, int H, int q_len, int splits) {
 
 }  // namespace
 
-size_t decode_workspace_size(int B, int H, int q_len, int num_sms) {
+size_t mma_workspace_size(int B, int H, int q_len, int num_sms) {
   return ws_bytes_for(B, H, q_len, splits_for(B, H, q_len, num_sms));
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   const int rows = a.H * a.q_len;
   if (a.B == 0 || rows == 0) return cudaSuccess;
   int splits = splits_for(a.B, a.H, a.q_len, a.num_sms);

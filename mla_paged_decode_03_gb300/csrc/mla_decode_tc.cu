@@ -1,0 +1,1049 @@
+// Split-KV paged MLA decode on the Blackwell tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// What it computes is the same as the warp-level kernel (mla_decode_mma.cu): query row i
+// of request b sees the global prefix G_i = max(0, G_b - (q_len-1-i)) ("vLLM PR #52188
+// (DSpark + DCP)" page, section "关键源码片段"), this shard holds
+// L_i = min(seq_lens[b], G_i / cp + (G_i % cp > rank)) of those keys, and
+// out = softmax(scale q K^T) V with V = K[:, :512], lse in base e or 2 ("vLLM PR #54012"
+// page, section "实现拆解" step 3; "vLLM PR #48180" page, section "实现拆解" step 1).
+//
+// Design.  A unit is 128 query rows of one request (rows ordered (q-row i, head h)); all
+// of them share every key, so S = Q K^T and O = P V are dense 128-row contractions.  The
+// fp32 accumulator O of 128 rows x 512 dims fills one SM's whole tensor memory, leaving
+// no room for S.  So each unit runs on a CTA pair (a cluster of two SMs):
+//
+//   CTA 0 (the S-CTA) keeps Q's 512 latent dims in TMEM as the A operand (256 columns),
+//     Q's 64 rope dims in shared memory, and two 64-column S buffers.  Per 64-key tile a
+//     TMA warp streams the keys (9 chunks of 64 keys x 64 dims, 128-byte swizzle) into
+//     shared memory, one thread issues 36 MMAs (M=128, N=64, K=16) into S, and four
+//     softmax warps (one query row per thread) read S, apply the per-row causal bound,
+//     keep the running max / sum (online softmax in base 2, the running max only moved
+//     when a tile's max exceeds it by more than 2^8), write P (bf16) into a swizzled
+//     shared-memory tile and bulk-copy it, with the per-row rescale factors, into CTA 1.
+//   CTA 1 (the O-CTA) holds O in all 512 TMEM columns.  A TMA warp streams the same keys'
+//     first 512 dims (V); one thread issues 8 MMAs (M=128, N=256, K=16) of P V per tile;
+//     four warps rescale O in TMEM on the rare tiles where the running max moved, and at
+//     the end of a segment read O out, scale by 1/l and store it.
+//
+// Both CTAs compute every key exactly once for QK (576 dims) and once for PV (512 dims).
+// Work is balanced statically: the 64-key tiles of all units are concatenated and cluster
+// c takes tiles [c*T/C, (c+1)*T/C); a unit cut between clusters leaves fp32 partials
+// (normalised out + base-2 LSE) in the workspace that the combine kernel merges.
+//
+// Safety: every wait is bounded (sm100.cuh); an abort word in each CTA (set on timeout,
+// also written into the peer) makes all roles stop; TMA loads never point outside the
+// cache (missing or invalid pages become out-of-range rows that TMA fills with zeros);
+// V rows past a request's keys are zeroed in shared memory before the PV MMA, so that
+// slots past seq_len (which may hold anything) never reach the accumulator.
+#include <math.h>
+#include <stdint.h>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+#include "../../include/mla_decode.h"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 576;
+constexpr int kDv = 512;
+constexpr int kM = 128;             // query rows per unit
+constexpr int kTile = 64;           // keys per tile
+constexpr int kChunkBytes = kTile * 128;      // 64 keys x 64 dims bf16 = 8 KB
+constexpr int kKChunks = 9;         // 8 latent + 1 rope chunks per tile (S-CTA)
+constexpr int kVChunks = 8;         // latent chunks per tile (O-CTA)
+constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
+constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
+constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr int kThreads = 256;
+constexpr int kEvCorrect = 1;
+constexpr int kEvFinal = 2;
+
+// shared memory layout (identical offsets in both CTAs of a pair)
+constexpr int kOffRing = 0;                                  // 2 x 9 x 8 KB (S) / 2 x 8 x 8 KB (O)
+constexpr int kOffQRope = kOffRing + 2 * kKChunks * kChunkBytes;   // 147456
+constexpr int kOffP = kOffQRope + kM * 128;                  // 163840
+constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 200704
+constexpr int kOffFinInvL = kOffBar + 1024;                  // 128 floats (O-CTA)
+constexpr int kOffMisc = kOffFinInvL + 512;                  // tmem base, abort, etc.
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slack
+
+// barrier indices (8 bytes each) inside [kOffBar, kOffBar + 1024)
+enum Bar : int {
+  // S-CTA
+  B_KFULL = 0,            // [2][9]
+  B_KEMPTY = 18,          // [2]
+  B_SFULL = 20,           // [2]
+  B_SFREE = 22,           // [2]
+  B_QREADY = 24,
+  B_QFREE = 25,
+  B_PFREE = 26,           // [2]  (arrived by the O-CTA's multicast commit)
+  // O-CTA
+  B_VFULL = 28,           // [2][8]
+  B_VEMPTY = 44,          // [2]
+  B_PFULL = 46,           // [2]  (completed by the S-CTA's bulk copy)
+  B_PVDONE = 48,
+  B_EV = 49,              // MMA warp -> correction warps: one event (rescale or final)
+  B_CORRDONE = 50,
+  B_OFINAL = 51,
+  B_OFREE = 52,
+  B_COUNT = 53
+};
+
+struct Params {
+  const uint16_t* q;
+  const int32_t* bt;
+  long long bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* gseq;
+  int B, H, q_len, bs, num_blocks, max_blocks, cp, rank;
+  int rows;            // H * q_len
+  int row_tiles;       // ceil(rows / 128)
+  int units;           // B * row_tiles
+  int clusters;        // C
+  int whole_units;     // 1: no workspace, each cluster takes whole units round-robin
+  int box_rows;        // rows per TMA box = min(bs, 64)
+  float scale_log2;
+  float lse_mul;
+  uint16_t* out;
+  float* lse;
+  int2* meta;          // [units] first / last cluster of each unit
+  float* ws_lse;       // [units + C][128]
+  float* ws_o;         // [units + C][128][512]
+  unsigned int* status;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t smem_base, int i) {
+  return smem_base + kOffBar + 8 * i;
+}
+
+// Keys visible to row r (0-based within the request's q_len*H rows).
+__device__ __forceinline__ int row_bound(const Params& p, int r, long long G, int cap) {
+  const int i = r / p.H;
+  long long Gi = G - (p.q_len - 1 - i);
+  if (Gi < 0) Gi = 0;
+  const long long loc = Gi / p.cp + ((Gi % p.cp) > p.rank ? 1 : 0);
+  return (int)(loc < cap ? loc : cap);
+}
+
+__device__ __forceinline__ int seq_cap(const Params& p, int b) {
+  int cap = __ldg(p.seq_lens + b);
+  const int lim = p.max_blocks * p.bs;
+  if (cap > lim) cap = lim;
+  return cap < 0 ? 0 : cap;
+}
+
+// Largest visible length over the rows of unit u (rows are ordered by q-row).
+__device__ __forceinline__ int unit_keys(const Params& p, int u) {
+  const int b = u / p.row_tiles, rt = u % p.row_tiles;
+  const int last_row = min((rt + 1) * kM, p.rows) - 1;
+  return row_bound(p, last_row, __ldg(p.gseq + b), seq_cap(p, b));
+}
+
+__device__ __forceinline__ int unit_tiles(const Params& p, int u) {
+  return (unit_keys(p, u) + kTile - 1) / kTile;
+}
+
+// Iterates the segments (unit, tile range) that cluster c owns, in order.  Each role of
+// both CTAs of the pair runs its own copy of the iterator and sees the same sequence.
+struct SegIter {
+  int u;            // current unit
+  int t_begin;      // first tile of the segment within the unit
+  int t_end;        // one past the last tile
+  long long g0;     // global index of the unit's first tile
+  long long g_end;  // end of this cluster's global tile range
+  int c;
+  int stride_units; // whole-unit mode: clusters
+  bool whole;
+  bool single;      // the segment covers the whole unit
+  int slot;         // workspace slot of a partial
+};
+
+__device__ __forceinline__ long long range_start(long long T, int c, int C) {
+  return T * c / C;
+}
+
+// Index of the cluster that owns global tile x.
+__device__ __forceinline__ int owner_of(long long x, long long T, int C) {
+  return (int)(((x + 1) * C - 1) / T);
+}
+
+// ---------------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------------
+struct SmemCtx {
+  uint32_t base;          // shared address of the aligned base
+  uint8_t* ptr;           // generic pointer of the aligned base
+  volatile int* abort;
+};
+
+__device__ __forceinline__ void set_abort_both(const SmemCtx& s, uint32_t peer) {
+  *s.abort = 1;
+  st_cluster_u32(mapa(s.base + kOffMisc + 4, peer), 1u);
+}
+
+// Bounded wait; on failure the abort word of both CTAs of the pair is set.
+__device__ __forceinline__ bool wait_bar(const SmemCtx& s, int i, uint32_t parity,
+                                         const Params& p, bool cluster_scope = false) {
+  if (mbar_wait(bar_addr(s.base, i), parity, s.abort, p.status, cluster_scope)) return true;
+  set_abort_both(s, cluster_ctarank() ^ 1u);
+  return false;
+}
+
+// First segment of cluster c (scan over units), or none.
+__device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int* s_scan) {
+  it.c = c;
+  it.whole = p.whole_units != 0;
+  if (it.whole) {
+    it.stride_units = p.clusters;
+    for (int u = c; u < p.units; u += p.clusters) {
+      const int nt = unit_tiles(p, u);
+      if (nt > 0) {
+        it.u = u;
+        it.t_begin = 0;
+        it.t_end = nt;
+        it.single = true;
+        it.slot = 0;
+        return true;
+      }
+    }
+    return false;
+  }
+  const long long a = range_start(T, c, p.clusters), e = range_start(T, c + 1, p.clusters);
+  if (a >= e) return false;
+  // s_scan holds the unit containing tile a and that unit's first global tile
+  it.u = s_scan[0];
+  it.g0 = ((long long)s_scan[2] << 32) | (unsigned)s_scan[1];
+  it.g_end = e;
+  const int nt = unit_tiles(p, it.u);
+  it.t_begin = (int)(a - it.g0);
+  it.t_end = (int)min((long long)nt, e - it.g0);
+  it.single = (it.t_begin == 0 && it.t_end == nt);
+  it.slot = it.u + c;
+  return true;
+}
+
+__device__ bool seg_next(const Params& p, SegIter& it) {
+  if (it.whole) {
+    for (int u = it.u + it.stride_units; u < p.units; u += it.stride_units) {
+      const int nt = unit_tiles(p, u);
+      if (nt > 0) {
+        it.u = u;
+        it.t_begin = 0;
+        it.t_end = nt;
+        return true;
+      }
+    }
+    return false;
+  }
+  long long g = it.g0 + it.t_end;      // next global tile
+  if (g >= it.g_end) return false;
+  int u = it.u;
+  long long g0 = it.g0 + unit_tiles(p, u);
+  ++u;
+  // skip units with no tiles
+  int nt = 0;
+  while (u < p.units) {
+    nt = unit_tiles(p, u);
+    if (nt > 0) break;
+    ++u;
+  }
+  if (u >= p.units) return false;
+  it.u = u;
+  it.g0 = g0;
+  it.t_begin = 0;
+  it.t_end = (int)min((long long)nt, it.g_end - g0);
+  it.single = (it.t_end == nt);
+  it.slot = u + it.c;
+  return true;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  SmemCtx s;
+  s.ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  s.base = smem_u32(s.ptr);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(s.ptr + kOffMisc);   // [0] tmem base, [1] abort
+  s.abort = reinterpret_cast<volatile int*>(misc + 1);
+  int* s_scan = reinterpret_cast<int*>(misc + 4);                     // [u, g0 lo, g0 hi]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t peer = crank ^ 1u;
+  const int c = (int)cluster_id_x();
+  const bool is_s = (crank == 0);
+
+  // ---- setup: barriers, TMEM, schedule scan -----------------------------------------
+  if (tid == 0) {
+    *s.abort = 0;
+    for (int i = 0; i < 18; ++i) mbar_init(bar_addr(s.base, B_KFULL + i), 1);
+    for (int i = 0; i < 16; ++i) mbar_init(bar_addr(s.base, B_VFULL + i), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_addr(s.base, B_KEMPTY + i), 1);
+      mbar_init(bar_addr(s.base, B_SFULL + i), 1);
+      mbar_init(bar_addr(s.base, B_SFREE + i), 4);
+      mbar_init(bar_addr(s.base, B_PFREE + i), 1);
+      mbar_init(bar_addr(s.base, B_VEMPTY + i), 1);
+      mbar_init(bar_addr(s.base, B_PFULL + i), 1);
+    }
+    mbar_init(bar_addr(s.base, B_QREADY), 4);
+    mbar_init(bar_addr(s.base, B_QFREE), 1);
+    mbar_init(bar_addr(s.base, B_PVDONE), 1);
+    mbar_init(bar_addr(s.base, B_EV), 1);
+    mbar_init(bar_addr(s.base, B_CORRDONE), 4);
+    mbar_init(bar_addr(s.base, B_OFINAL), 1);
+    mbar_init(bar_addr(s.base, B_OFREE), 4);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s.base + kOffMisc, 512);
+    tmem_relinquish();
+  }
+
+  // schedule: total tiles T and the unit holding this cluster's first tile
+  long long T = 0;
+  {
+    __shared__ long long s_total;
+    __shared__ int s_warp[kThreads / 32];
+    const long long a_start_guess = -1;
+    (void)a_start_guess;
+    if (tid == 0) {
+      s_total = 0;
+      s_scan[0] = -1;
+    }
+    __syncthreads();
+    // pass 1: T
+    long long local = 0;
+    for (int u = tid; u < p.units; u += kThreads) local += unit_tiles(p, u);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)local);
+    __syncthreads();
+    T = s_total;
+    if (!p.whole_units && T > 0) {
+      const long long a = range_start(T, c, p.clusters);
+      // pass 2: chunked exclusive scan to find the unit containing tile a
+      long long running = 0;
+      for (int base = 0; base < p.units; base += kThreads) {
+        const int u = base + tid;
+        const int nt = u < p.units ? unit_tiles(p, u) : 0;
+        int incl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        int wpre = 0, total = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+          if (w < warp) wpre += s_warp[w];
+          total += s_warp[w];
+        }
+        const long long excl = running + wpre + incl - nt;
+        if (u < p.units && nt > 0 && excl <= a && a < excl + nt) {
+          s_scan[0] = u;
+          s_scan[1] = (int)(excl & 0xffffffffLL);
+          s_scan[2] = (int)(excl >> 32);
+        }
+        running += total;
+        __syncthreads();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();          // barrier inits visible cluster-wide before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  // meta for the combine: the owner of a unit's first tile records its cluster range
+  if (is_s && tid == 0 && !p.whole_units && T > 0 && p.meta != nullptr) {
+    SegIter it;
+    if (seg_first(p, c, it, T, s_scan)) {
+      do {
+        if (it.t_begin == 0) {
+          const int nt = unit_tiles(p, it.u);
+          const int cf = c, cl = owner_of(it.g0 + nt - 1, T, p.clusters);
+          p.meta[it.u] = make_int2(cf, cl);
+        }
+      } while (seg_next(p, it));
+    }
+  }
+
+  const float kNegInf = -INFINITY;
+
+  if (is_s) {
+    // ============================== S-CTA ==========================================
+    if (warp == 0 && lane == 0) {
+      // ---- K producer ---------------------------------------------------------------
+      SegIter it;
+      long long n = 0;      // global tile counter of this cluster
+      bool bad = false;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          const int b = it.u / p.row_tiles;
+          const int keys = unit_keys(p, it.u);
+          const int seg_keys = min(keys, it.t_end * kTile);
+          const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
+          for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
+            const int g = (int)(n & 1);
+            if (!wait_bar(s, B_KEMPTY + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
+            const int t0 = t * kTile;
+            for (int ch = 0; ch < kKChunks; ++ch) {
+              const uint32_t fb = bar_addr(s.base, B_KFULL + g * 9 + ch);
+              mbar_arrive_expect_tx(fb, kChunkBytes);
+              const uint32_t dst = s.base + kOffRing + (g * 9 + ch) * kChunkBytes;
+              for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
+                const int tok = t0 + r0;
+                int y = p.num_blocks * p.bs;       // past the cache: zero fill
+                if (tok < seg_keys) {
+                  const int page = __ldg(btrow + tok / p.bs);
+                  if (page >= 0 && page < p.num_blocks)
+                    y = page * p.bs + tok % p.bs;
+                  else
+                    bad = true;
+                }
+                tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
+              }
+            }
+          }
+        } while (!*s.abort && seg_next(p, it));
+      }
+      if (bad) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+      if (*s.abort) {
+        // let loads already issued land before the CTA exits
+        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
+          for (int ch = 0; ch < kKChunks; ++ch)
+            mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(k & 1) * 9 + ch), (uint32_t)((k >> 1) & 1));
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---- QK MMA issuer ------------------------------------------------------------
+      SegIter it;
+      long long n = 0;
+      int nseg = 0;
+      const uint32_t idesc = idesc_bf16(kM, kTile, false, false);
+      const uint32_t qrope = s.base + kOffQRope;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          if (!wait_bar(s, B_QREADY, (uint32_t)(nseg & 1), p)) break;
+          tc_fence_after();
+          for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
+            const int g = (int)(n & 1);
+            if (!wait_bar(s, B_SFREE + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + 256 + g * kTile;
+            bool ok = true;
+            for (int ch = 0; ch < kKChunks && ok; ++ch) {
+              ok = wait_bar(s, B_KFULL + g * 9 + ch, (uint32_t)((n >> 1) & 1), p);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t kb = s.base + kOffRing + (g * 9 + ch) * kChunkBytes;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t bdesc = smem_desc(kb + 32 * k, 16, 1024, kSwizzle128B);
+                if (ch < 8)
+                  mma_ts(d, tmem + ch * 32 + k * 8, bdesc, idesc, (ch | k) != 0);
+                else
+                  mma_ss(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128B), bdesc, idesc, 1);
+              }
+            }
+            if (!ok) break;
+            mma_commit(bar_addr(s.base, B_KEMPTY + g));
+            mma_commit(bar_addr(s.base, B_SFULL + g));
+          }
+          if (*s.abort) break;
+          mma_commit(bar_addr(s.base, B_QFREE));
+          ++nseg;
+        } while (seg_next(p, it));
+      }
+    } else if (warp >= 4) {
+      // ---- softmax warps: thread = query row -----------------------------------------
+      const int r = tid - 128;                      // row within the unit, = TMEM lane
+      const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+      const bool leader = (r == 0);
+      SegIter it;
+      long long n = 0;
+      int nseg = 0;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          const int b = it.u / p.row_tiles, rt = it.u % p.row_tiles;
+          const int row = rt * kM + r;
+          const bool valid = row < p.rows;
+          const long long G = __ldg(p.gseq + b);
+          const int cap = seq_cap(p, b);
+          const int Lr = valid ? row_bound(p, row, G, cap) : 0;
+          const int seg_end_tok = it.t_end * kTile;
+          const int lim_row = min(Lr, seg_end_tok);
+
+          // Q of this unit: latent dims into TMEM cols 0..255, rope dims into smem
+          if (nseg > 0 && !wait_bar(s, B_QFREE, (uint32_t)((nseg - 1) & 1), p)) break;
+          {
+            const uint4* qrow = reinterpret_cast<const uint4*>(
+                p.q + ((long long)b * p.rows + (valid ? row : 0)) * kD);
+            for (int c32 = 0; c32 < 8; ++c32) {
+              uint32_t v[32];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                uint4 x = valid ? __ldg(qrow + c32 * 8 + k) : make_uint4(0, 0, 0, 0);
+                v[4 * k] = x.x;
+                v[4 * k + 1] = x.y;
+                v[4 * k + 2] = x.z;
+                v[4 * k + 3] = x.w;
+              }
+              tmem_st32(tmem + lane_off + c32 * 32, v);
+            }
+            uint8_t* rope = s.ptr + kOffQRope + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 x = valid ? __ldg(qrow + 64 + j) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(rope + ((j ^ (r & 7)) << 4)) = x;
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(s.base, B_QREADY));
+          }
+
+          float m_ref = kNegInf, l = 0.f;
+          bool aborted = false;
+          for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
+            const int g = (int)(n & 1);
+            const int j = (int)(n & 1);            // P slot
+            if (!wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p)) {
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+            uint32_t sv[64];
+            {
+              uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv);
+              uint32_t (&b2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
+              tmem_ld32(tmem + lane_off + 256 + g * kTile, a);
+              tmem_ld32(tmem + lane_off + 256 + g * kTile + 32, b2);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(s.base, B_SFREE + g));
+
+            const int t0 = t * kTile;
+            const int lim = lim_row - t0;          // valid keys of this row in the tile
+            float x[64];
+            float tmax = kNegInf;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+              x[k] = k < lim ? __uint_as_float(sv[k]) * p.scale_log2 : kNegInf;
+              tmax = fmaxf(tmax, x[k]);
+            }
+            float alpha = 1.f;
+            bool resc = false;
+            if (tmax > m_ref + kRescaleThreshold) {
+              if (m_ref != kNegInf) {
+                alpha = exp2f(m_ref - tmax);
+                resc = true;
+              }
+              l *= alpha;
+              m_ref = tmax;
+            }
+            const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float e0 = exp2f(x[2 * k] - mu), e1 = exp2f(x[2 * k + 1] - mu);
+              __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
+              sum += e0 + e1;
+              pk[k] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            l += sum;
+            const bool last = (t + 1 == it.t_end);
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+
+            // staging slot j must no longer be read by the bulk copy issued two tiles ago
+            if (leader) bulk_wait_read<1>();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
+            uint8_t* prow = slot + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            float* side = reinterpret_cast<float*>(slot + kPBytes);
+            side[r] = alpha;
+            side[128 + r] = (last && l > 0.f) ? 1.f / l : 0.f;
+            int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
+            if (lane == 0) flags[warp - 4] = any_resc ? 1 : 0;
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (leader) {
+              if (!wait_bar(s, B_PFREE + j, (uint32_t)(((n >> 1) + 1) & 1), p, true)) {
+                set_abort_both(s, peer);
+              } else {
+                const uint32_t rbar = mapa(bar_addr(s.base, B_PFULL + j), peer);
+                mbar_arrive_expect_tx_cluster(rbar, kPBytes + kSideBytes);
+                bulk_s2cluster(mapa(s.base + kOffP + j * kPSlotBytes, peer),
+                               s.base + kOffP + j * kPSlotBytes, kPBytes + kSideBytes, rbar);
+                bulk_commit();
+              }
+            }
+            if (last && valid) {
+              const float lse2 = l > 0.f ? m_ref + log2f(l) : kNegInf;
+              const long long grow = (long long)b * p.rows + row;
+              if (it.single) {
+                if (p.lse != nullptr) p.lse[grow] = lse2 * p.lse_mul;
+              } else {
+                p.ws_lse[(long long)it.slot * kM + r] = lse2;
+              }
+            }
+          }
+          if (aborted || *s.abort) break;
+          ++nseg;
+        } while (seg_next(p, it));
+      }
+      if (leader) bulk_wait<0>();
+      // drain: the O-CTA's last two PV commits arrive on this CTA's p_free barriers
+      if (leader && n > 0 && !*s.abort) {
+        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
+          wait_bar(s, B_PFREE + (int)(k & 1), (uint32_t)((k >> 1) & 1), p, true);
+      }
+    }
+  } else {
+    // ============================== O-CTA ==========================================
+    if (warp == 0 && lane == 0) {
+      // ---- V producer -----------------------------------------------------------------
+      SegIter it;
+      long long n = 0;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          const int b = it.u / p.row_tiles;
+          const int keys = unit_keys(p, it.u);
+          const int seg_keys = min(keys, it.t_end * kTile);
+          const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
+          for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
+            const int g = (int)(n & 1);
+            if (!wait_bar(s, B_VEMPTY + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
+            const int t0 = t * kTile;
+            for (int ch = 0; ch < kVChunks; ++ch) {
+              const uint32_t fb = bar_addr(s.base, B_VFULL + g * 8 + ch);
+              mbar_arrive_expect_tx(fb, kChunkBytes);
+              const uint32_t dst = s.base + kOffRing + (g * 8 + ch) * kChunkBytes;
+              for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
+                const int tok = t0 + r0;
+                int y = p.num_blocks * p.bs;
+                if (tok < seg_keys) {
+                  const int page = __ldg(btrow + tok / p.bs);
+                  if (page >= 0 && page < p.num_blocks) y = page * p.bs + tok % p.bs;
+                }
+                tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
+              }
+            }
+          }
+        } while (!*s.abort && seg_next(p, it));
+      }
+      if (*s.abort) {
+        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
+          for (int ch = 0; ch < kVChunks; ++ch)
+            mbar_wait_drain(bar_addr(s.base, B_VFULL + (int)(k & 1) * 8 + ch), (uint32_t)((k >> 1) & 1));
+      }
+    } else if (warp == 1) {
+      // ---- PV MMA issuer (lane 0 issues; the warp zeroes V rows past the keys) ---------
+      SegIter it;
+      long long n = 0;
+      long long pv_waited = 0;       // PV commits already waited for on B_PVDONE
+      int nseg = 0;
+      const uint32_t idesc = idesc_bf16(kM, 256, false, true);
+      float* fin = reinterpret_cast<float*>(s.ptr + kOffFinInvL);
+      volatile int* ev_word = reinterpret_cast<volatile int*>(misc + 8);
+      int ncorr = 0;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          const int keys = unit_keys(p, it.u);
+          const int seg_keys = min(keys, it.t_end * kTile);
+          if (nseg > 0 && !wait_bar(s, B_OFREE, (uint32_t)((nseg - 1) & 1), p)) break;
+          tc_fence_after();
+          bool ok = true;
+          for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
+            const int g = (int)(n & 1), j = (int)(n & 1);
+            ok = wait_bar(s, B_PFULL + j, (uint32_t)((n >> 1) & 1), p, true);
+            if (!ok) break;
+            const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
+            const int* flags = reinterpret_cast<const int*>(slot + kPBytes + 1024);
+            const bool first = (t == it.t_begin);
+            const bool last = (t + 1 == it.t_end);
+            const bool resc = !first && (flags[0] | flags[1] | flags[2] | flags[3]);
+            if (last) {
+              const float* side = reinterpret_cast<const float*>(slot + kPBytes);
+              for (int k = lane; k < kM; k += 32) fin[k] = side[128 + k];
+              __syncwarp();
+            }
+            if (resc) {
+              // every PV issued so far must be complete before O is rescaled
+              while (ok && pv_waited < n) {
+                ok = wait_bar(s, B_PVDONE, (uint32_t)(pv_waited & 1), p);
+                ++pv_waited;
+              }
+              if (!ok) break;
+              if (lane == 0) {
+                *ev_word = kEvCorrect | (j << 8);
+                mbar_arrive(bar_addr(s.base, B_EV));
+              }
+              ok = wait_bar(s, B_CORRDONE, (uint32_t)(ncorr & 1), p);
+              ++ncorr;
+              if (!ok) break;
+              tc_fence_after();
+            }
+            for (int ch = 0; ch < kVChunks && ok; ++ch)
+              ok = wait_bar(s, B_VFULL + g * 8 + ch, (uint32_t)((n >> 1) & 1), p);
+            if (!ok) break;
+            const int t0 = t * kTile;
+            const int valid_keys = seg_keys - t0;
+            if (valid_keys < kTile) {
+              // zero V rows [valid_keys, 64) of all chunks (whole 128-byte rows)
+              const int r_lo = valid_keys < 0 ? 0 : valid_keys;
+              for (int ch = 0; ch < kVChunks; ++ch) {
+                uint8_t* base = s.ptr + kOffRing + (g * 8 + ch) * kChunkBytes;
+                for (int idx = r_lo * 8 + lane; idx < kTile * 8; idx += 32) {
+                  const int rr = idx >> 3, q = idx & 7;
+                  *reinterpret_cast<uint4*>(base + (rr >> 3) * 1024 + (rr & 7) * 128 + q * 16) =
+                      make_uint4(0, 0, 0, 0);
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t pa = s.base + kOffP + j * kPSlotBytes;
+              const uint32_t vb = s.base + kOffRing + g * 8 * kChunkBytes;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t adesc = smem_desc(pa + 32 * k, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint64_t bdesc =
+                      smem_desc(vb + h * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024, kSwizzle128B);
+                  mma_ss(tmem + h * 256, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
+                }
+              }
+              mma_commit(bar_addr(s.base, B_VEMPTY + g));
+              mma_commit_multicast(bar_addr(s.base, B_PFREE + j), (uint16_t)1);
+              mma_commit(bar_addr(s.base, B_PVDONE));
+              if (last) {
+                mma_commit(bar_addr(s.base, B_OFINAL));
+                *ev_word = kEvFinal;
+                mbar_arrive(bar_addr(s.base, B_EV));
+              }
+            }
+            __syncwarp();
+          }
+          if (!ok || *s.abort) break;
+          ++nseg;
+        } while (seg_next(p, it));
+      }
+      // drain the PV commits before teardown
+      while (!*s.abort && pv_waited < n) {
+        if (!wait_bar(s, B_PVDONE, (uint32_t)(pv_waited & 1), p)) break;
+        ++pv_waited;
+      }
+    } else if (warp >= 4) {
+      // ---- correction / epilogue warps: thread = row ---------------------------------
+      const int r = tid - 128;
+      const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+      const float* fin = reinterpret_cast<const float*>(s.ptr + kOffFinInvL);
+      volatile int* ev_word = reinterpret_cast<volatile int*>(misc + 8);
+      SegIter it;
+      int nseg = 0, nev = 0;
+      if (seg_first(p, c, it, T, s_scan)) {
+        do {
+          const int b = it.u / p.row_tiles, rt = it.u % p.row_tiles;
+          const int row = rt * kM + r;
+          const bool valid = row < p.rows;
+          bool ok = true;
+          // events from the MMA warp: rescale requests, then the segment's final one
+          for (;;) {
+            ok = wait_bar(s, B_EV, (uint32_t)(nev & 1), p);
+            ++nev;
+            if (!ok) break;
+            const int ev = *ev_word;
+            if ((ev & 0xff) == kEvFinal) break;
+            const int j = (ev >> 8) & 1;
+            const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
+            tc_fence_after();
+            const float a = reinterpret_cast<const float*>(slot + kPBytes)[r];
+            if (__any_sync(0xffffffffu, a != 1.f)) {
+              for (int c32 = 0; c32 < 16; ++c32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + c32 * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
+                tmem_st32(tmem + lane_off + c32 * 32, v);
+              }
+              tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(s.base, B_CORRDONE));
+          }
+          if (!ok) break;
+          // epilogue: O * (1/l) -> out (single segment) or fp32 partial
+          ok = wait_bar(s, B_OFINAL, (uint32_t)(nseg & 1), p);
+          if (!ok) break;
+          tc_fence_after();
+          const float inv = fin[r];
+          for (int c32 = 0; c32 < 16; ++c32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + c32 * 32, v);
+            tmem_wait_ld();
+            if (!valid) continue;
+            if (it.single) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)b * p.rows + row) * kDv +
+                                                    c32 * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                                           __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+                  w[e] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + ((long long)it.slot * kM + r) * kDv +
+                                                      c32 * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                     __uint_as_float(v[4 * q + 2]) * inv,
+                                     __uint_as_float(v[4 * q + 3]) * inv);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_addr(s.base, B_OFREE));
+          ++nseg;
+        } while (!*s.abort && seg_next(p, it));
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the partials of units that were cut between clusters; units with no visible key
+// get out = 0 and lse = -inf.  One warp per (unit, row).
+__global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= (long long)p.units * kM) return;
+  const int u = (int)(wid / kM), r = (int)(wid % kM);
+  const int b = u / p.row_tiles, rt = u % p.row_tiles;
+  const int row = rt * kM + r;
+  if (row >= p.rows) return;
+  const long long grow = (long long)b * p.rows + row;
+  const int nt = unit_tiles(p, u);
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kDv;
+  if (nt == 0) {
+    *reinterpret_cast<uint4*>(o + 8 * lane) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(o + 256 + 8 * lane) = make_uint4(0, 0, 0, 0);
+    if (p.lse != nullptr && lane == 0) p.lse[grow] = -INFINITY;
+    return;
+  }
+  if (p.whole_units) return;
+  const int2 m = p.meta[u];
+  if (m.x == m.y) return;                     // one cluster wrote the final result
+  float mx = -INFINITY;
+  for (int cc = m.x + lane; cc <= m.y; cc += 32)
+    mx = fmaxf(mx, p.ws_lse[(long long)(u + cc) * kM + r]);
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int cc = m.x; cc <= m.y; ++cc) {
+      const float w = exp2f(p.ws_lse[(long long)(u + cc) * kM + r] - mx);
+      if (w == 0.f) continue;
+      wsum += w;
+      const float* src = p.ws_o + ((long long)(u + cc) * kM + r) * kDv;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(src + 256 * h + 8 * lane));
+        const float4 c4 = __ldcs(reinterpret_cast<const float4*>(src + 256 * h + 8 * lane + 4));
+        acc[8 * h + 0] = fmaf(w, a.x, acc[8 * h + 0]);
+        acc[8 * h + 1] = fmaf(w, a.y, acc[8 * h + 1]);
+        acc[8 * h + 2] = fmaf(w, a.z, acc[8 * h + 2]);
+        acc[8 * h + 3] = fmaf(w, a.w, acc[8 * h + 3]);
+        acc[8 * h + 4] = fmaf(w, c4.x, acc[8 * h + 4]);
+        acc[8 * h + 5] = fmaf(w, c4.y, acc[8 * h + 5]);
+        acc[8 * h + 6] = fmaf(w, c4.z, acc[8 * h + 6]);
+        acc[8 * h + 7] = fmaf(w, c4.w, acc[8 * h + 7]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 hh = __floats2bfloat162_rn(acc[8 * h + 2 * e] * inv, acc[8 * h + 2 * e + 1] * inv);
+      w4[e] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(o + 256 * h + 8 * lane) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+  if (p.lse != nullptr && lane == 0)
+    p.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * p.lse_mul : -INFINITY;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+size_t tc_ws_bytes(int units, int clusters) {
+  const size_t slots = (size_t)units + clusters;
+  size_t b = ((size_t)units * sizeof(int2) + 255) / 256 * 256;
+  b += (slots * kM * sizeof(float) + 255) / 256 * 256;
+  b += slots * kM * kDv * sizeof(float);
+  return b;
+}
+
+int tc_clusters(int num_sms) { return num_sms / 2 > 0 ? num_sms / 2 : 1; }
+
+}  // namespace
+
+bool tc_supported(const DecodeArgs& a) {
+  const int bs = a.block_size;
+  if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128)) return false;
+  if ((long long)a.num_blocks * bs + 64 >= (1LL << 31)) return false;
+  if (reinterpret_cast<uintptr_t>(a.kv) % 16 != 0) return false;
+  return get_encoder() != nullptr;
+}
+
+size_t tc_workspace_size(int B, int H, int q_len, int num_sms) {
+  const int rt = (H * q_len + kM - 1) / kM;
+  return tc_ws_bytes(B * rt, tc_clusters(num_sms));
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
+  Params p;
+  p.q = a.q;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.seq_lens = a.seq_lens;
+  p.gseq = a.gseq;
+  p.B = a.B;
+  p.H = a.H;
+  p.q_len = a.q_len;
+  p.bs = a.block_size;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks = a.max_blocks;
+  p.cp = a.cp_world;
+  p.rank = a.cp_rank;
+  p.rows = a.H * a.q_len;
+  p.row_tiles = (p.rows + kM - 1) / kM;
+  p.units = a.B * p.row_tiles;
+  p.box_rows = a.block_size < 64 ? a.block_size : 64;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.lse_mul = a.lse_base_e ? 0.6931471805599453f : 1.0f;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.status = a.status;
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {false};
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int C = tc_clusters(a.num_sms);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, mla_decode_tc_kernel, &cfg) == cudaSuccess &&
+        active > 0 && active < C)
+      C = active;
+    cudaGetLastError();
+  }
+  p.clusters = C;
+  const size_t need = tc_ws_bytes(p.units, C);
+  if (a.workspace != nullptr && a.workspace_bytes >= need) {
+    char* ws = static_cast<char*>(a.workspace);
+    const size_t slots = (size_t)p.units + C;
+    p.meta = reinterpret_cast<int2*>(ws);
+    ws += ((size_t)p.units * sizeof(int2) + 255) / 256 * 256;
+    p.ws_lse = reinterpret_cast<float*>(ws);
+    ws += (slots * kM * sizeof(float) + 255) / 256 * 256;
+    p.ws_o = reinterpret_cast<float*>(ws);
+    p.whole_units = 0;
+  } else {
+    p.meta = nullptr;
+    p.ws_lse = nullptr;
+    p.ws_o = nullptr;
+    p.whole_units = 1;
+    if (C > p.units) C = p.units;
+    p.clusters = C;
+  }
+
+  CUtensorMap map;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.num_blocks * a.block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = get_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                               const_cast<uint16_t*>(a.kv), dims, strides, box, es,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(map, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long warps = (long long)p.units * kM;
+  mla_tc_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

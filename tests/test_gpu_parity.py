@@ -26,6 +26,15 @@ DEV = "cuda"
 def _clean_status():
     M.device_status()
     yield
+    M.set_decode_kernel(M.KERNEL_AUTO)
+
+
+@pytest.fixture(params=["mma", "tc"])
+def kernel(request):
+    """Runs a decode test once per decode kernel (warp-level mma.sync, tcgen05)."""
+    prev = M.set_decode_kernel(M.KERNEL_MMA if request.param == "mma" else M.KERNEL_TC)
+    yield request.param
+    M.set_decode_kernel(prev)
 
 
 # ---------------------------------------------------------------------------
@@ -159,11 +168,11 @@ def _check_workload(w, relative=False, with_workspace=True):
     assert M.device_status() == 0
 
 
-def test_decode_tiny_full():
+def test_decode_tiny_full(kernel):
     _check_workload(synth.make_workload("tiny"))
 
 
-def test_decode_cp2_full():
+def test_decode_cp2_full(kernel):
     _check_workload(synth.make_workload("cp2"))
 
 
@@ -172,11 +181,11 @@ def test_decode_cp2_full():
     ("spec", [3000, 1234]),
     ("long", [5000, 4097]),
 ])
-def test_decode_reduced_workloads(name, lengths):
+def test_decode_reduced_workloads(name, lengths, kernel):
     _check_workload(synth.make_workload(name, lengths=lengths), relative=(name == "long"))
 
 
-def test_decode_without_workspace_matches():
+def test_decode_without_workspace_matches(kernel):
     _check_workload(synth.make_workload("plain", lengths=[1500, 3000]), with_workspace=False)
 
 
@@ -186,18 +195,18 @@ def test_decode_without_workspace_matches():
     (1, [191, 192, 193], 3), (8, [40, 300], 2),
 ])
 @pytest.mark.parametrize("H_,bs", [(16, 16), (64, 64), (128, 64)])
-def test_decode_edge_cases(q_len, lengths, cp, H_, bs):
+def test_decode_edge_cases(q_len, lengths, cp, H_, bs, kernel):
     w = synth.make_custom(len(lengths), H_, q_len, lengths, bs, cp, base_e=(cp != 4),
                           seed=q_len * 100 + cp + H_)
     _check_workload(w)
 
 
-def test_decode_block_table_with_wide_stride():
+def test_decode_block_table_with_wide_stride(kernel):
     w = synth.make_custom(2, 64, 2, [300, 129], 64, 2, seed=5, spare_columns=9)
     _check_workload(w)
 
 
-def test_decode_bad_page_is_flagged_not_read():
+def test_decode_bad_page_is_flagged_not_read(kernel):
     w = synth.make_custom(2, 16, 1, [40, 40], 16, 1, seed=9)
     step = _gpu_shards(w)
     bt = step.block_table.clone()
@@ -211,7 +220,7 @@ def test_decode_bad_page_is_flagged_not_read():
     assert torch.isfinite(out[1].float()).all()
 
 
-def test_decode_seq_len_beyond_table_is_flagged():
+def test_decode_seq_len_beyond_table_is_flagged(kernel):
     w = synth.make_custom(1, 16, 1, [40], 16, 1, seed=10)
     step = _gpu_shards(w)
     step.seq_lens[0] = torch.tensor([10_000], dtype=torch.int32, device=DEV)
