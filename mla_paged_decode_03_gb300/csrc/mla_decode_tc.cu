@@ -114,6 +114,7 @@ struct Params {
   float lse_mul;
   uint16_t* out;
   float* lse;
+  long long* hdr;      // workspace header: [0] = total tiles T of this call
   int2* meta;          // [units] first / last cluster of each unit
   float* ws_lse;       // [units + C][128]
   float* ws_o;         // [units + C][128][512]
@@ -363,7 +364,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  // meta for the combine: the owner of a unit's first tile records its cluster range
+  // meta for the combine: the owner of a unit's first tile records its cluster range;
+  // cluster 0 records T so that the combine can skip clusters with an empty tile range
+  if (is_s && tid == 0 && c == 0 && !p.whole_units && p.hdr != nullptr) p.hdr[0] = T;
   if (is_s && tid == 0 && !p.whole_units && T > 0 && p.meta != nullptr) {
     SegIter it;
     if (seg_first(p, c, it, T, s_scan)) {
@@ -858,6 +861,8 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   const int row = rt * kM + r;
   if (row >= p.rows) return;
   const long long grow = (long long)b * p.rows + row;
+  if (rt == 0 && r == 0 && lane == 0 && __ldg(p.seq_lens + b) > p.max_blocks * p.bs)
+    atomicOr(p.status, MLA_STATUS_SEQ_TOO_LONG);
   const int nt = unit_tiles(p, u);
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kDv;
   if (nt == 0) {
@@ -869,9 +874,15 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   if (p.whole_units) return;
   const int2 m = p.meta[u];
   if (m.x == m.y) return;                     // one cluster wrote the final result
+  // clusters between the first and the last owner hold a partial unless their tile
+  // range is empty (possible when there are fewer tiles than clusters)
+  const long long T = p.hdr[0];
+  auto holds = [&](int cc) {
+    return range_start(T, cc, p.clusters) < range_start(T, cc + 1, p.clusters);
+  };
   float mx = -INFINITY;
   for (int cc = m.x + lane; cc <= m.y; cc += 32)
-    mx = fmaxf(mx, p.ws_lse[(long long)(u + cc) * kM + r]);
+    if (holds(cc)) mx = fmaxf(mx, p.ws_lse[(long long)(u + cc) * kM + r]);
 #pragma unroll
   for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
   float acc[16];
@@ -880,6 +891,7 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   float wsum = 0.f;
   if (mx != -INFINITY) {
     for (int cc = m.x; cc <= m.y; ++cc) {
+      if (!holds(cc)) continue;
       const float w = exp2f(p.ws_lse[(long long)(u + cc) * kM + r] - mx);
       if (w == 0.f) continue;
       wsum += w;
@@ -929,7 +941,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 
 size_t tc_ws_bytes(int units, int clusters) {
   const size_t slots = (size_t)units + clusters;
-  size_t b = ((size_t)units * sizeof(int2) + 255) / 256 * 256;
+  size_t b = 256;                                        // header
+  b += ((size_t)units * sizeof(int2) + 255) / 256 * 256;
   b += (slots * kM * sizeof(float) + 255) / 256 * 256;
   b += slots * kM * kDv * sizeof(float);
   return b;
@@ -1010,6 +1023,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   if (a.workspace != nullptr && a.workspace_bytes >= need) {
     char* ws = static_cast<char*>(a.workspace);
     const size_t slots = (size_t)p.units + C;
+    p.hdr = reinterpret_cast<long long*>(ws);
+    ws += 256;
     p.meta = reinterpret_cast<int2*>(ws);
     ws += ((size_t)p.units * sizeof(int2) + 255) / 256 * 256;
     p.ws_lse = reinterpret_cast<float*>(ws);
@@ -1017,6 +1032,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     p.ws_o = reinterpret_cast<float*>(ws);
     p.whole_units = 0;
   } else {
+    p.hdr = nullptr;
     p.meta = nullptr;
     p.ws_lse = nullptr;
     p.ws_o = nullptr;

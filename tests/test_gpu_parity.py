@@ -29,6 +29,13 @@ def _clean_status():
     M.set_decode_kernel(M.KERNEL_AUTO)
 
 
+@pytest.fixture(autouse=True)
+def _status_clear():
+    """Every test starts with a clean device status word."""
+    M.device_status()
+    yield
+
+
 @pytest.fixture(params=["mma", "tc"])
 def kernel(request):
     """Runs a decode test once per decode kernel (warp-level mma.sync, tcgen05)."""
@@ -109,10 +116,10 @@ def test_cp_local_slot_padded_table_stride():
 
 def test_cp_local_slot_out_of_table_flags_status():
     bt = torch.tensor([[3, 5]], dtype=torch.int32, device=DEV)
-    pos = torch.tensor([[0, 1, 63, 64, 65, 1000, -2]], dtype=torch.int64, device=DEV)
+    pos = torch.tensor([[0, 1, 62, 63, 64, 65, 1000, -2]], dtype=torch.int64, device=DEV)
     got = M.cp_local_slot(pos, bt, 16, 2, 0).cpu().numpy()[0]
-    assert list(got[3:]) == [-1, -1, -1, -1]              # virtual block 2+ is past the table
-    assert list(got[:3]) == [48, -1, 5 * 16 + 15]
+    assert list(got[4:]) == [-1, -1, -1, -1]              # virtual block 2+ is past the table
+    assert list(got[:4]) == [48, -1, 5 * 16 + 15, -1]     # 63 is rank 1's
     assert M.device_status() & 4
 
 
