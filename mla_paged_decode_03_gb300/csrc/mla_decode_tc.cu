@@ -660,7 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- PV MMA issuer (lane 0 issues; the warp zeroes V rows past the keys) ---------
       SegIter it;
       long long n = 0;
-      long long pv_waited = 0;       // PV commits already waited for on B_PVDONE
+      long long pv_phase = 0;        // phases of B_PVDONE waited for (one per fresh commit)
       int nseg = 0;
       const uint32_t idesc = idesc_bf16(kM, 256, false, true);
       float* fin = reinterpret_cast<float*>(s.ptr + kOffFinInvL);
@@ -688,11 +688,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               __syncwarp();
             }
             if (resc) {
-              // every PV issued so far must be complete before O is rescaled
-              while (ok && pv_waited < n) {
-                ok = wait_bar(s, B_PVDONE, (uint32_t)(pv_waited & 1), p);
-                ++pv_waited;
-              }
+              // every PV issued so far must be complete before O is rescaled: one fresh
+              // commit tracks all of them
+              if (lane == 0) mma_commit(bar_addr(s.base, B_PVDONE));
+              __syncwarp();
+              ok = wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p);
+              ++pv_phase;
               if (!ok) break;
               if (lane == 0) {
                 *ev_word = kEvCorrect | (j << 8);
@@ -738,7 +739,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
               mma_commit(bar_addr(s.base, B_VEMPTY + g));
               mma_commit_multicast(bar_addr(s.base, B_PFREE + j), (uint16_t)1);
-              mma_commit(bar_addr(s.base, B_PVDONE));
               if (last) {
                 mma_commit(bar_addr(s.base, B_OFINAL));
                 *ev_word = kEvFinal;
@@ -751,10 +751,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++nseg;
         } while (seg_next(p, it));
       }
-      // drain the PV commits before teardown
-      while (!*s.abort && pv_waited < n) {
-        if (!wait_bar(s, B_PVDONE, (uint32_t)(pv_waited & 1), p)) break;
-        ++pv_waited;
+      // every PV complete before teardown
+      if (n > 0 && !*s.abort) {
+        if (lane == 0) mma_commit(bar_addr(s.base, B_PVDONE));
+        __syncwarp();
+        wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p);
+        ++pv_phase;
       }
     } else if (warp >= 4) {
       // ---- correction / epilogue warps: thread = row ---------------------------------

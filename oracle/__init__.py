@@ -6,6 +6,7 @@ product library.
 """
 from .mla_ref import (  # noqa: F401
     PAD_SLOT_ID,
+    ref_abs_weighted,
     ref_attention_global,
     ref_build_pool,
     ref_cp_local_slot,

@@ -133,6 +133,33 @@ def _softmax_attend(q_rows: np.ndarray, keys: np.ndarray, scale: float):
     return p @ keys[:, :D_V], lse
 
 
+def ref_abs_weighted(q, kv_rows, G, q_len: int, cp_world: int, cp_rank: int, scale: float,
+                     rows=None, row_getter=None):
+    """Error scale of a softmax-weighted sum, not a result: sum_l softmax(s)_l |V_l| per
+    (row, head, dim) over the keys shard ``cp_rank`` holds (same visibility as
+    ref_mla_decode_global).  A kernel that rounds the softmax weights to bf16 (8
+    significant bits, round to nearest) perturbs each weight by at most 2^-9 of itself,
+    so its output error is bounded by 2^-9 times this quantity; shards combine it with
+    the same LSE weights as their outputs."""
+    q = np.asarray(q)
+    B, ql, H, D = q.shape
+    G = np.asarray(G, dtype=np.int64)
+    out = np.zeros((B * q_len, H, D_V), dtype=np.float64)
+    todo = rows if rows is not None else [(b, i) for b in range(B) for i in range(q_len)]
+    for b, i in todo:
+        Gi = int(ref_row_global_prefix(G[b], q_len)[i])
+        idx = np.arange(cp_rank, Gi, cp_world, dtype=np.int64)
+        if idx.size == 0:
+            continue
+        keys = (row_getter(b, idx) if row_getter is not None
+                else np.asarray(kv_rows[b], dtype=np.float64)[idx])
+        keys = np.asarray(keys, dtype=np.float64)
+        s = scale * (np.asarray(q[b, i], dtype=np.float64) @ keys.T)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        out[b * q_len + i] = (e / e.sum(axis=1, keepdims=True)) @ np.abs(keys[:, :D_V])
+    return out
+
+
 def ref_gather_pages(kv_cache, block_table_row, L: int) -> np.ndarray:
     """Rows 0..L-1 of one request's shard-local sequence: local position l lives at
     page block_table_row[l // block_size], offset l % block_size ([#54012] section

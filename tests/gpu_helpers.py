@@ -3,9 +3,15 @@ element-wise comparisons with the tolerances of the decode contract.
 
 Tolerances: bf16 outputs within max-abs 2e-2 of the float64 oracle; fp32 LSEs within
 1e-3 absolute.  For the long-context workload (1% of KV rows x20, so |out| reaches tens)
-the output bound is relative per element, |gpu - ref| <= 2e-2 * max(1, |ref|), because a
-bf16 result there has a half-ulp of up to 0.125 and an absolute 2e-2 cannot hold even
-for a correctly rounded value.
+the output bound is per element
+    |gpu - ref| <= 2e-2 * max(1, |ref|) + 2^-8 * A,   A = sum_l softmax(s)_l |V_l|,
+because (1) a bf16 result there has a half-ulp of up to 0.125, so an absolute 2e-2
+cannot hold even for a correctly rounded value, and (2) the tensor-core PV product takes
+the softmax weights in bf16, which moves each weight by up to 2^-9 of itself: with a few
+x20 keys sharing the weight, an output element near zero can be a difference of terms
+of size ~50, whose bf16-weight error (bounded by 2^-9 A) exceeds 2e-2 although every
+step is correctly rounded.  A is computed by the oracle (ref_abs_weighted); a wrong key
+or a wrong weight moves the result by O(|V|), far above 2^-8 A.
 """
 from __future__ import annotations
 
@@ -24,14 +30,15 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, relative=False, what=""):
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, relative=False, what="", abs_weighted=None):
     og = f64(out_gpu)
     lg = f64(lse_gpu)
     assert og.shape == out_ref.shape, (og.shape, out_ref.shape)
     assert np.all(np.isfinite(og)), f"{what}: non-finite output"
     err = np.abs(og - out_ref)
     if relative:
-        err = err / np.maximum(1.0, np.abs(out_ref))
+        assert abs_weighted is not None
+        err = err / (np.maximum(1.0, np.abs(out_ref)) + abs_weighted * (2.0 ** -8) / OUT_TOL)
     worst = float(err.max()) if err.size else 0.0
     assert worst <= OUT_TOL, f"{what}: out error {worst:.3e} > {OUT_TOL}"
     fin = np.isfinite(lse_ref)
@@ -48,12 +55,13 @@ def oracle_workload_rows(w):
     return q, rows
 
 
-def oracle_shards(w):
-    """Per-shard (out, lse) over oracle-built pools, plus the merged result."""
+def oracle_shards(w, with_abs=False):
+    """Per-shard (out, lse) over oracle-built pools, plus the merged result; with
+    ``with_abs`` also the per-shard and merged ref_abs_weighted error scales."""
     q, rows = oracle_workload_rows(w)
     bt = w.block_table.numpy()
     G = w.G.numpy()
-    outs, lses = [], []
+    outs, lses, absw = [], [], []
     for r in range(w.cp):
         pool = R.ref_build_pool(rows, bt, w.bs, w.cp, r, w.num_blocks)
         sl = R.ref_local_len(G, w.cp, r)
@@ -61,8 +69,13 @@ def oracle_shards(w):
                                 w.scale, w.base_e)
         outs.append(o)
         lses.append(l)
+        if with_abs:
+            absw.append(R.ref_abs_weighted(q, rows, G, w.q_len, w.cp, r, w.scale))
     mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), w.base_e)
-    return outs, lses, mo, ml
+    if not with_abs:
+        return outs, lses, mo, ml
+    ma, _ = R.ref_lse_merge(np.stack(absw), np.stack(lses), w.base_e)
+    return outs, lses, mo, ml, absw, ma
 
 
 def device_row_getter(w):
@@ -76,8 +89,13 @@ def device_row_getter(w):
     return get
 
 
-def oracle_sampled_shard(w, sample, rank, getter):
+def oracle_sampled_shard(w, sample, rank, getter, with_abs=False):
     """Shard ``rank``'s result for sampled (b, i) rows, stated on global positions."""
     q = f64(w.q)
-    return R.ref_mla_decode_global(q, None, w.G.numpy(), w.q_len, w.cp, rank, w.scale,
+    o, l = R.ref_mla_decode_global(q, None, w.G.numpy(), w.q_len, w.cp, rank, w.scale,
                                    w.base_e, rows=sample, row_getter=getter)
+    if not with_abs:
+        return o, l
+    a = R.ref_abs_weighted(q, None, w.G.numpy(), w.q_len, w.cp, rank, w.scale, rows=sample,
+                           row_getter=getter)
+    return o, l, a

@@ -347,8 +347,20 @@ def check_end_aligned_mask_differs():
     assert differs
 
 
+def check_abs_weighted_closed_form():
+    """With non-negative V the error scale sum_l p_l |V_l| is the output itself."""
+    q, rows = make_small_case(41, 2, 3, 2, (40, 77), 8)
+    rows = [np.abs(r) for r in rows]
+    G = np.array([40, 77])
+    for cp, rank in ((1, 0), (3, 2)):
+        o, _ = R.ref_mla_decode_global(q, rows, G, 2, cp, rank, 0.1, True)
+        a = R.ref_abs_weighted(q, rows, G, 2, cp, rank, 0.1)
+        assert np.max(np.abs(o - a)) < 1e-12
+
+
 ALL_CHECKS = [check_slot_golden, check_local_len_golden, check_local_len_bruteforce,
               check_row_prefix_positions, check_slot_bruteforce, check_decode_vs_sdpa,
               check_decode_bruteforce_tiny, check_merge_closed_form, check_lse_bases,
               check_merge_equals_unsharded, check_pool_vs_global_formulation,
-              check_flattened_equals_native, check_end_aligned_mask_differs]
+              check_flattened_equals_native, check_end_aligned_mask_differs,
+              check_abs_weighted_closed_form]

@@ -167,11 +167,16 @@ def _check_workload(w, relative=False, with_workspace=True):
     step = _gpu_shards(w, with_workspace)
     out, lse = step.run()
     torch.cuda.synchronize()
-    ro, rl, mo, ml = H.oracle_shards(w)
+    if relative:
+        ro, rl, mo, ml, ra, ma = H.oracle_shards(w, with_abs=True)
+    else:
+        ro, rl, mo, ml = H.oracle_shards(w)
+        ra, ma = [None] * w.cp, None
     if w.cp > 1:
         for r in range(w.cp):
-            H.compare(step.partials[r], step.lses[r], ro[r], rl[r], relative, f"{w.name} shard {r}")
-    H.compare(out, lse, mo, ml, relative, f"{w.name} merged")
+            H.compare(step.partials[r], step.lses[r], ro[r], rl[r], relative,
+                      f"{w.name} shard {r}", ra[r])
+    H.compare(out, lse, mo, ml, relative, f"{w.name} merged", ma)
     assert M.device_status() == 0
 
 
@@ -247,18 +252,19 @@ def _sampled_full(name, sample, relative=False):
     torch.cuda.synchronize()
     assert M.device_status() == 0
     get = H.device_row_getter(w)
-    outs, lses = [], []
+    outs, lses, absw = [], [], []
+    idx = [b * w.q_len + i for b, i in sample]
     for r in range(w.cp):
-        o, l = H.oracle_sampled_shard(w, sample, r, get)
+        o, l, a = H.oracle_sampled_shard(w, sample, r, get, with_abs=True)
         outs.append(o)
         lses.append(l)
+        absw.append(a)
         if r < 2 and w.cp > 1:
-            idx = [b * w.q_len + i for b, i in sample]
             H.compare(step.partials[r][idx], step.lses[r][idx], o[idx], l[idx], relative,
-                      f"{name} shard {r}")
+                      f"{name} shard {r}", a[idx])
     mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), w.base_e)
-    idx = [b * w.q_len + i for b, i in sample]
-    H.compare(out[idx], lse[idx], mo[idx], ml[idx], relative, f"{name} merged")
+    ma, _ = R.ref_lse_merge(np.stack(absw), np.stack(lses), w.base_e)
+    H.compare(out[idx], lse[idx], mo[idx], ml[idx], relative, f"{name} merged", ma[idx])
     # properties that hold for every row: finite outputs, |out| bounded by max |V|
     assert torch.isfinite(out.float()).all()
     assert torch.isfinite(lse).all()
