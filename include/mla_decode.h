@@ -148,6 +148,33 @@ int cp_local_slot(const int64_t* positions, const int32_t* block_table, int64_t 
                   int interleave, int64_t* slots, mla_stream_t stream);
 
 /*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call.  It computes exactly what mla_decode
+ * computes, with the same arguments minus the workspace: some callers cannot call
+ * cudaMalloc or any allocating routine on their decode path (a runtime whose memory is
+ * planned once at start-up, a host program that links only this C library and owns no
+ * allocator), yet split-KV needs scratch for its per-split partial results.  This call
+ * takes that scratch from one fixed 64 MiB array that the library declares in device
+ * memory; every GPU that loads the library holds the array until the process exits.
+ *   - A problem whose split-KV scratch exceeds 64 MiB is rejected with
+ *     MLA_ERR_UNSUPPORTED (message in mla_last_error) and nothing is launched.
+ *   - All calls on a device share the array and it keeps the last call's contents;
+ *     calls whose kernels overlap on the GPU (other streams or host threads) race on it
+ *     and must be serialised.  Nothing in it needs to start at zero.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ * Errors: as mla_decode, plus MLA_ERR_UNSUPPORTED for the size limit.
+ */
+int mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                       int64_t bt_stride, const int32_t* seq_lens,
+                       const int32_t* causal_seqlens_global, int B, int H, int q_len,
+                       int block_size, int num_blocks, int max_blocks, int cp_world,
+                       int cp_rank, float scale, void* out, float* lse, int lse_base_e,
+                       mla_stream_t stream);
+
+/*
  * Waits for `stream`, then reads and clears the current device's status word.
  * Returns MLA_OK when no kernel flagged anything since the last call, MLA_ERR_DEVICE
  * when one did (mla_last_error() names the bits; *bits_out receives them if non-NULL),

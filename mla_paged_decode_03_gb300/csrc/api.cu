@@ -67,6 +67,16 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+namespace mla {
+int api_fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+}  // namespace mla
+
 extern "C" {
 
 int mla_abi_version(void) { return (1 << 16) | 0; }

@@ -15,6 +15,12 @@ size_t decode_workspace_size(int B, int H, int q_len, int num_sms) {
   return a > b ? a : b;
 }
 
+size_t decode_workspace_for(int B, int H, int q_len, int num_sms, int block_size) {
+  const bool tc_bs = block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
+  if (g_choice != 1 && tc_bs) return tc_workspace_size(B, H, q_len, num_sms);
+  return mma_workspace_size(B, H, q_len, num_sms);
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B == 0 || a.H * a.q_len == 0) return cudaSuccess;
   const bool tc = g_choice == 2 || (g_choice == 0 && tc_supported(a));

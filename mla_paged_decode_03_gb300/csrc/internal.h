@@ -41,6 +41,12 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 size_t mma_workspace_size(int B, int H, int q_len, int num_sms);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
 
+// Split-KV scratch the kernel chosen for this block size uses at its preferred split.
+size_t decode_workspace_for(int B, int H, int q_len, int num_sms, int block_size);
+
+// Records a message for mla_last_error() and returns `code` (api.cu).
+int api_fail(int code, const char* fmt, ...);
+
 // Testing hook: 0 = automatic choice, 1 = force the warp-level kernel, 2 = force tcgen05.
 void set_decode_kernel_choice(int choice);
 
