@@ -146,11 +146,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
-def time_config(name, steps, warmup, device, flush, with_e2e=False, event_calls=True):
+def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None):
     import mla_paged_decode_03_gb300 as m
     from mla_paged_decode_03_gb300.layer_step import DcpDecodeStep
 
-    w = synth.make_workload(name, device=device)
+    w = synth.make_workload(name, device=device, B=batch)
     step = DcpDecodeStep.from_workload(w, device)
     del w.kv_global
     stream = torch.cuda.current_stream()
@@ -340,7 +340,8 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     wall0 = time.perf_counter()
-    res = time_config(args.config, args.steps, args.warmup, device, flush, with_e2e=True)
+    res = time_config(args.config, args.steps, args.warmup, device, flush, with_e2e=True,
+                      batch=args.batch)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     s = summarize(res, pk)
@@ -361,7 +362,8 @@ def run_ours(args):
                 "unit": "GB/s", "frac": s["decode_call_gbs"] / pk["hbm"]}
     roof.update({"traffic": None, "kernel": "mla_decode call (split-KV decode + split combine)",
                  "peak_source": pk["source"] + " (burst)"})
-    cpu = cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline) else None
+    cpu = (cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline
+                                                  and args.batch is None) else None)
     line = {
         "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
@@ -423,6 +425,8 @@ def main():
     ap.add_argument("--config", default="cp2", choices=synth.ORDER)
     ap.add_argument("--extra-configs", default="tiny,plain,spec,long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the headline workload's batch (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
