@@ -83,7 +83,7 @@ size_t mla_decode_workspace_size(int B, int H, int q_len, int num_sms);
  *   causal_seqlens_global  int32 [B] global lengths; may be NULL only if cp_world == 1,
  *                then seq_lens is used.
  *   B >= 0, 1 <= H, 1 <= q_len <= MLA_MAX_Q_LEN, block_size >= 1, num_blocks >= 1,
- *   1 <= max_blocks <= bt_stride, 1 <= cp_world, 0 <= cp_rank < cp_world, finite scale.
+ *   1 <= max_blocks <= bt_stride, 1 <= cp_world, 0 <= cp_rank < cp_world, finite scale > 0.
  *   out          bf16 [B*q_len, H, 512], 16-byte aligned.
  *   lse          float [B*q_len, H] or NULL.
  *   workspace    device scratch of workspace_bytes (may be NULL / 0), 256-byte aligned.

@@ -121,7 +121,8 @@ int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
   if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world)
     return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: need 0 <= cp_rank (%d) < cp_world (%d)",
                 cp_rank, cp_world);
-  if (!isfinite(scale)) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: scale not finite");
+  if (!isfinite(scale) || !(scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: scale must be finite and > 0");
   if (B == 0) return ok();
   if (!q || !kv_cache || !block_table || !seq_lens || !out)
     return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: null q/kv_cache/block_table/seq_lens/out");

@@ -198,6 +198,34 @@ __device__ __forceinline__ bool wait_bar(const SmemCtx& s, int i, uint32_t parit
   return false;
 }
 
+// 2^x on the SFU (ex2.approx, flush-to-zero); arguments here are <= 2^8 or -inf.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// A wait's outcome made uniform across the warp (every lane waited itself).
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+// The same across the 128 threads of warps 4..7 (named barrier 2), so that no thread of
+// the group leaves a loop that the others stay in (they meet again at named barriers).
+__device__ __forceinline__ bool group_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.and.pred q, 2, 128, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
 // First segment of cluster c (scan over units), or none.
 __device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int* s_scan) {
   it.c = c;
@@ -426,8 +454,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int ch = 0; ch < kKChunks; ++ch)
             mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(k & 1) * 9 + ch), (uint32_t)((k >> 1) & 1));
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---- QK MMA issuer ------------------------------------------------------------
+    } else if (warp == 1) {
+      // ---- QK MMA issuer (the whole warp runs the loop; one elected lane issues) --------
       SegIter it;
       long long n = 0;
       int nseg = 0;
@@ -435,16 +463,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t qrope = s.base + kOffQRope;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
-          if (!wait_bar(s, B_QREADY, (uint32_t)(nseg & 1), p)) break;
+          if (!warp_all(wait_bar(s, B_QREADY, (uint32_t)(nseg & 1), p))) break;
           tc_fence_after();
-          for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
+          bool ok = true;
+          for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
             const int g = (int)(n & 1);
-            if (!wait_bar(s, B_SFREE + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
+            ok = warp_all(wait_bar(s, B_SFREE + g, (uint32_t)(((n >> 1) + 1) & 1), p));
+            if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + 256 + g * kTile;
-            bool ok = true;
             for (int ch = 0; ch < kKChunks && ok; ++ch) {
-              ok = wait_bar(s, B_KFULL + g * 9 + ch, (uint32_t)((n >> 1) & 1), p);
+              ok = warp_all(wait_bar(s, B_KFULL + g * 9 + ch, (uint32_t)((n >> 1) & 1), p));
               if (!ok) break;
               tc_fence_after();
               const uint32_t kb = s.base + kOffRing + (g * 9 + ch) * kChunkBytes;
@@ -452,17 +481,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 4; ++k) {
                 const uint64_t bdesc = smem_desc(kb + 32 * k, 16, 1024, kSwizzle128B);
                 if (ch < 8)
-                  mma_ts(d, tmem + ch * 32 + k * 8, bdesc, idesc, (ch | k) != 0);
+                  mma_ts_warp(d, tmem + ch * 32 + k * 8, bdesc, idesc, (ch | k) != 0);
                 else
-                  mma_ss(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128B), bdesc, idesc, 1);
+                  mma_ss_warp(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128B), bdesc, idesc, 1);
               }
             }
             if (!ok) break;
-            mma_commit(bar_addr(s.base, B_KEMPTY + g));
-            mma_commit(bar_addr(s.base, B_SFULL + g));
+            mma_commit_warp(bar_addr(s.base, B_KEMPTY + g));
+            mma_commit_warp(bar_addr(s.base, B_SFULL + g));
           }
-          if (*s.abort) break;
-          mma_commit(bar_addr(s.base, B_QFREE));
+          if (!ok || !warp_all(*s.abort == 0)) break;
+          mma_commit_warp(bar_addr(s.base, B_QFREE));
           ++nseg;
         } while (seg_next(p, it));
       }
@@ -486,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int lim_row = min(Lr, seg_end_tok);
 
           // Q of this unit: latent dims into TMEM cols 0..255, rope dims into smem
-          if (nseg > 0 && !wait_bar(s, B_QFREE, (uint32_t)((nseg - 1) & 1), p)) break;
+          if (nseg > 0 && !group_all(wait_bar(s, B_QFREE, (uint32_t)((nseg - 1) & 1), p))) break;
           {
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 p.q + ((long long)b * p.rows + (valid ? row : 0)) * kD);
@@ -520,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
             const int g = (int)(n & 1);
             const int j = (int)(n & 1);            // P slot
-            if (!wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p)) {
+            if (!group_all(wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p))) {
               aborted = true;
               break;
             }
@@ -539,33 +568,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
             const int t0 = t * kTile;
             const int lim = lim_row - t0;          // valid keys of this row in the tile
-            float x[64];
-            float tmax = kNegInf;
+            // running max on the raw scores (scale > 0 keeps the order), in log2 units;
+            // 8 independent max / sum chains keep one warp per SMSP from stalling on
+            // dependent adds
+            float mx8[8];
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
-              x[k] = k < lim ? __uint_as_float(sv[k]) * p.scale_log2 : kNegInf;
-              tmax = fmaxf(tmax, x[k]);
+            for (int q = 0; q < 8; ++q) mx8[q] = kNegInf;
+            if (lim >= kTile) {
+#pragma unroll
+              for (int k = 0; k < kTile; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
+            } else {
+#pragma unroll
+              for (int k = 0; k < kTile; ++k)
+                if (k < lim) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
             }
+            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float tmax = smax * p.scale_log2;
             float alpha = 1.f;
             bool resc = false;
             if (tmax > m_ref + kRescaleThreshold) {
               if (m_ref != kNegInf) {
-                alpha = exp2f(m_ref - tmax);
+                alpha = fast_exp2(m_ref - tmax);
                 resc = true;
               }
               l *= alpha;
               m_ref = tmax;
             }
-            const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-            float sum = 0.f;
-            uint32_t pk[32];
+            const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
+            float sum8[8];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const float e0 = exp2f(x[2 * k] - mu), e1 = exp2f(x[2 * k + 1] - mu);
-              __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
-              sum += e0 + e1;
-              pk[k] = *reinterpret_cast<uint32_t*>(&h);
+            for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
+            uint32_t pk[32];
+            if (lim >= kTile) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu));
+                const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu));
+                sum8[k & 7] += e0 + e1;
+                pk[k] = pack_bf16x2(e0, e1);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float e0 = 2 * k < lim
+                    ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu)) : 0.f;
+                const float e1 = 2 * k + 1 < lim
+                    ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu)) : 0.f;
+                sum8[k & 7] += e0 + e1;
+                pk[k] = pack_bf16x2(e0, e1);
+              }
             }
+            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l += sum;
             const bool last = (t + 1 == it.t_end);
             const bool any_resc = __any_sync(0xffffffffu, resc);
@@ -607,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (aborted || *s.abort) break;
+          if (aborted || !group_all(*s.abort == 0)) break;
           ++nseg;
         } while (seg_next(p, it));
       }
@@ -670,12 +725,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         do {
           const int keys = unit_keys(p, it.u);
           const int seg_keys = min(keys, it.t_end * kTile);
-          if (nseg > 0 && !wait_bar(s, B_OFREE, (uint32_t)((nseg - 1) & 1), p)) break;
+          if (nseg > 0 && !warp_all(wait_bar(s, B_OFREE, (uint32_t)((nseg - 1) & 1), p))) break;
           tc_fence_after();
           bool ok = true;
           for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
             const int g = (int)(n & 1), j = (int)(n & 1);
-            ok = wait_bar(s, B_PFULL + j, (uint32_t)((n >> 1) & 1), p, true);
+            ok = warp_all(wait_bar(s, B_PFULL + j, (uint32_t)((n >> 1) & 1), p, true));
             if (!ok) break;
             const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
             const int* flags = reinterpret_cast<const int*>(slot + kPBytes + 1024);
@@ -690,22 +745,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (resc) {
               // every PV issued so far must be complete before O is rescaled: one fresh
               // commit tracks all of them
-              if (lane == 0) mma_commit(bar_addr(s.base, B_PVDONE));
-              __syncwarp();
-              ok = wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p);
+              mma_commit_warp(bar_addr(s.base, B_PVDONE));
+              ok = warp_all(wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p));
               ++pv_phase;
               if (!ok) break;
               if (lane == 0) {
                 *ev_word = kEvCorrect | (j << 8);
                 mbar_arrive(bar_addr(s.base, B_EV));
               }
-              ok = wait_bar(s, B_CORRDONE, (uint32_t)(ncorr & 1), p);
+              ok = warp_all(wait_bar(s, B_CORRDONE, (uint32_t)(ncorr & 1), p));
               ++ncorr;
               if (!ok) break;
               tc_fence_after();
             }
             for (int ch = 0; ch < kVChunks && ok; ++ch)
-              ok = wait_bar(s, B_VFULL + g * 8 + ch, (uint32_t)((n >> 1) & 1), p);
+              ok = warp_all(wait_bar(s, B_VFULL + g * 8 + ch, (uint32_t)((n >> 1) & 1), p));
             if (!ok) break;
             const int t0 = t * kTile;
             const int valid_keys = seg_keys - t0;
@@ -723,8 +777,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
             }
-            if (lane == 0) {
-              tc_fence_after();
+            __syncwarp();
+            tc_fence_after();
+            {
               const uint32_t pa = s.base + kOffP + j * kPSlotBytes;
               const uint32_t vb = s.base + kOffRing + g * 8 * kChunkBytes;
 #pragma unroll
@@ -734,28 +789,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < 2; ++h) {
                   const uint64_t bdesc =
                       smem_desc(vb + h * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024, kSwizzle128B);
-                  mma_ss(tmem + h * 256, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
+                  mma_ss_warp(tmem + h * 256, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
                 }
               }
-              mma_commit(bar_addr(s.base, B_VEMPTY + g));
-              mma_commit_multicast(bar_addr(s.base, B_PFREE + j), (uint16_t)1);
-              if (last) {
-                mma_commit(bar_addr(s.base, B_OFINAL));
-                *ev_word = kEvFinal;
-                mbar_arrive(bar_addr(s.base, B_EV));
-              }
+              mma_commit_warp(bar_addr(s.base, B_VEMPTY + g));
+              mma_commit_multicast_warp(bar_addr(s.base, B_PFREE + j), (uint16_t)1);
+              if (last) mma_commit_warp(bar_addr(s.base, B_OFINAL));
+            }
+            if (last && lane == 0) {
+              *ev_word = kEvFinal;
+              mbar_arrive(bar_addr(s.base, B_EV));
             }
             __syncwarp();
           }
-          if (!ok || *s.abort) break;
+          if (!ok || !warp_all(*s.abort == 0)) break;
           ++nseg;
         } while (seg_next(p, it));
       }
       // every PV complete before teardown
-      if (n > 0 && !*s.abort) {
-        if (lane == 0) mma_commit(bar_addr(s.base, B_PVDONE));
-        __syncwarp();
-        wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p);
+      if (n > 0 && warp_all(*s.abort == 0)) {
+        mma_commit_warp(bar_addr(s.base, B_PVDONE));
+        warp_all(wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p));
         ++pv_phase;
       }
     } else if (warp >= 4) {
@@ -774,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bool ok = true;
           // events from the MMA warp: rescale requests, then the segment's final one
           for (;;) {
-            ok = wait_bar(s, B_EV, (uint32_t)(nev & 1), p);
+            ok = warp_all(wait_bar(s, B_EV, (uint32_t)(nev & 1), p));
             ++nev;
             if (!ok) break;
             const int ev = *ev_word;
@@ -800,7 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           // epilogue: O * (1/l) -> out (single segment) or fp32 partial
-          ok = wait_bar(s, B_OFINAL, (uint32_t)(nseg & 1), p);
+          ok = warp_all(wait_bar(s, B_OFINAL, (uint32_t)(nseg & 1), p));
           if (!ok) break;
           tc_fence_after();
           const float inv = fin[r];
@@ -837,7 +891,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_addr(s.base, B_OFREE));
           ++nseg;
-        } while (!*s.abort && seg_next(p, it));
+        } while (warp_all(*s.abort == 0) && seg_next(p, it));
       }
     }
   }

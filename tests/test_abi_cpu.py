@@ -75,6 +75,8 @@ def _decode(lib, **kw):
     (dict(cp=0), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(rank=-1), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(scale=float("nan")), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(scale=0.0), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(scale=-0.1), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(q=None), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(out=None), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(cp=2, gseq=None), _lib.MLA_ERR_INVALID_ARGUMENT),
