@@ -13,17 +13,20 @@
 // no room for S.  So each unit runs on a CTA pair (a cluster of two SMs):
 //
 //   CTA 0 (the S-CTA) keeps Q's 512 latent dims in TMEM as the A operand (256 columns),
-//     Q's 64 rope dims in shared memory, and two 64-column S buffers.  Per 64-key tile a
-//     TMA warp streams the keys (9 chunks of 64 keys x 64 dims, 128-byte swizzle) into
-//     shared memory, one thread issues 36 MMAs (M=128, N=64, K=16) into S, and four
-//     softmax warps (one query row per thread) read S, apply the per-row causal bound,
-//     keep the running max / sum (online softmax in base 2, the running max only moved
-//     when a tile's max exceeds it by more than 2^8), write P (bf16) into a swizzled
-//     shared-memory tile and bulk-copy it, with the per-row rescale factors, into CTA 1.
+//     Q's 64 rope dims in shared memory, and two 64-column S buffers.  A TMA warp streams
+//     the keys (9 chunks of 64 keys x 64 dims per tile, 128-byte swizzle) through a ring
+//     of 21 chunk slots, each freed as soon as its MMAs complete; the MMA warp issues 36
+//     MMAs (M=128, N=64, K=16) per tile into S; four softmax warps (one query row per
+//     thread) read S, apply the per-row causal bound, keep the running max / sum (online
+//     softmax in base 2, the running max only moved when a tile's max exceeds it by more
+//     than 2^8), write P (bf16) into a swizzled shared-memory tile and bulk-copy it, with
+//     the per-row rescale factors, into CTA 1.
 //   CTA 1 (the O-CTA) holds O in all 512 TMEM columns.  A TMA warp streams the same keys'
-//     first 512 dims (V); one thread issues 8 MMAs (M=128, N=256, K=16) of P V per tile;
-//     four warps rescale O in TMEM on the rare tiles where the running max moved, and at
-//     the end of a segment read O out, scale by 1/l and store it.
+//     first 512 dims (V) through five half-tile groups; the MMA warp issues 8 MMAs (M=128,
+//     N=256, K=16) of P V per tile; four warps rescale O in TMEM on the rare tiles where
+//     the running max moved, and at the end of a segment read O out, scale by 1/l and
+//     store it.
+//   Both MMA warps run their loops as whole converged warps and issue through elect.sync.
 //
 // Both CTAs compute every key exactly once for QK (576 dims) and once for PV (512 dims).
 // Work is balanced statically: the 64-key tiles of all units are concatenated and cluster
@@ -57,7 +60,8 @@ constexpr int kM = 128;             // query rows per unit
 constexpr int kTile = 64;           // keys per tile
 constexpr int kChunkBytes = kTile * 128;      // 64 keys x 64 dims bf16 = 8 KB
 constexpr int kKChunks = 9;         // 8 latent + 1 rope chunks per tile (S-CTA)
-constexpr int kVChunks = 8;         // latent chunks per tile (O-CTA)
+constexpr int kKSlots = 21;         // S-CTA key ring: 21 chunk slots (2.33 tiles), freed per chunk
+constexpr int kVGroups = 5;         // O-CTA value ring: 5 half-tile groups of 4 chunks (2.5 tiles)
 constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
 constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
 constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
@@ -67,10 +71,10 @@ constexpr int kEvCorrect = 1;
 constexpr int kEvFinal = 2;
 
 // shared memory layout (identical offsets in both CTAs of a pair)
-constexpr int kOffRing = 0;                                  // 2 x 9 x 8 KB (S) / 2 x 8 x 8 KB (O)
-constexpr int kOffQRope = kOffRing + 2 * kKChunks * kChunkBytes;   // 147456
-constexpr int kOffP = kOffQRope + kM * 128;                  // 163840
-constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 200704
+constexpr int kOffRing = 0;                                  // 21 x 8 KB (S) / 5 x 32 KB (O)
+constexpr int kOffQRope = kOffRing + kKSlots * kChunkBytes;  // 172032
+constexpr int kOffP = kOffQRope + kM * 128;                  // 188416
+constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 225280
 constexpr int kOffFinInvL = kOffBar + 1024;                  // 128 floats (O-CTA)
 constexpr int kOffMisc = kOffFinInvL + 512;                  // tmem base, abort, etc.
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slack
@@ -78,23 +82,23 @@ constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slac
 // barrier indices (8 bytes each) inside [kOffBar, kOffBar + 1024)
 enum Bar : int {
   // S-CTA
-  B_KFULL = 0,            // [2][9]
-  B_KEMPTY = 18,          // [2]
-  B_SFULL = 20,           // [2]
-  B_SFREE = 22,           // [2]
-  B_QREADY = 24,
-  B_QFREE = 25,
-  B_PFREE = 26,           // [2]  (arrived by the O-CTA's multicast commit)
+  B_KFULL = 0,            // [21] per key chunk slot
+  B_KEMPTY = 21,          // [21]
+  B_SFULL = 42,           // [2]
+  B_SFREE = 44,           // [2]
+  B_QREADY = 46,
+  B_QFREE = 47,
+  B_PFREE = 48,           // [2]  (arrived by the O-CTA's multicast commit)
   // O-CTA
-  B_VFULL = 28,           // [2][8]
-  B_VEMPTY = 44,          // [2]
-  B_PFULL = 46,           // [2]  (completed by the S-CTA's bulk copy)
-  B_PVDONE = 48,
-  B_EV = 49,              // MMA warp -> correction warps: one event (rescale or final)
-  B_CORRDONE = 50,
-  B_OFINAL = 51,
-  B_OFREE = 52,
-  B_COUNT = 53
+  B_VFULL = 50,           // [5] per half-tile value group
+  B_VEMPTY = 55,          // [5]
+  B_PFULL = 60,           // [2]  (completed by the S-CTA's bulk copy)
+  B_PVDONE = 62,
+  B_EV = 63,              // MMA warp -> correction warps: one event (rescale or final)
+  B_CORRDONE = 64,
+  B_OFINAL = 65,
+  B_OFREE = 66,
+  B_COUNT = 67
 };
 
 struct Params {
@@ -313,14 +317,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup: barriers, TMEM, schedule scan -----------------------------------------
   if (tid == 0) {
     *s.abort = 0;
-    for (int i = 0; i < 18; ++i) mbar_init(bar_addr(s.base, B_KFULL + i), 1);
-    for (int i = 0; i < 16; ++i) mbar_init(bar_addr(s.base, B_VFULL + i), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(bar_addr(s.base, B_KFULL + i), 1);
       mbar_init(bar_addr(s.base, B_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < kVGroups; ++i) {
+      mbar_init(bar_addr(s.base, B_VFULL + i), 1);
+      mbar_init(bar_addr(s.base, B_VEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(s.base, B_SFULL + i), 1);
       mbar_init(bar_addr(s.base, B_SFREE + i), 4);
       mbar_init(bar_addr(s.base, B_PFREE + i), 1);
-      mbar_init(bar_addr(s.base, B_VEMPTY + i), 1);
       mbar_init(bar_addr(s.base, B_PFULL + i), 1);
     }
     mbar_init(bar_addr(s.base, B_QREADY), 4);
@@ -416,6 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- K producer ---------------------------------------------------------------
       SegIter it;
       long long n = 0;      // global tile counter of this cluster
+      long long issued = 0; // key chunks issued
       bool bad = false;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
@@ -424,13 +433,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int seg_keys = min(keys, it.t_end * kTile);
           const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
           for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
-            const int g = (int)(n & 1);
-            if (!wait_bar(s, B_KEMPTY + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
             const int t0 = t * kTile;
-            for (int ch = 0; ch < kKChunks; ++ch) {
-              const uint32_t fb = bar_addr(s.base, B_KFULL + g * 9 + ch);
+            bool okk = true;
+            for (int ch = 0; ch < kKChunks && okk; ++ch) {
+              const long long m = n * kKChunks + ch;          // chunk sequence number
+              const int slot = (int)(m % kKSlots);
+              okk = wait_bar(s, B_KEMPTY + slot, (uint32_t)(((m / kKSlots) + 1) & 1), p);
+              if (!okk) break;
+              const uint32_t fb = bar_addr(s.base, B_KFULL + slot);
               mbar_arrive_expect_tx(fb, kChunkBytes);
-              const uint32_t dst = s.base + kOffRing + (g * 9 + ch) * kChunkBytes;
+              const uint32_t dst = s.base + kOffRing + slot * kChunkBytes;
               for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
                 const int tok = t0 + r0;
                 int y = p.num_blocks * p.bs;       // past the cache: zero fill
@@ -443,16 +455,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
               }
+              issued = m + 1;
             }
+            if (!okk) break;
           }
         } while (!*s.abort && seg_next(p, it));
       }
       if (bad) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
       if (*s.abort) {
         // let loads already issued land before the CTA exits
-        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
-          for (int ch = 0; ch < kKChunks; ++ch)
-            mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(k & 1) * 9 + ch), (uint32_t)((k >> 1) & 1));
+        for (long long m = (issued > kKSlots ? issued - kKSlots : 0); m < issued; ++m)
+          mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(m % kKSlots)), (uint32_t)((m / kKSlots) & 1));
       }
     } else if (warp == 1) {
       // ---- QK MMA issuer (the whole warp runs the loop; one elected lane issues) --------
@@ -473,10 +486,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t d = tmem + 256 + g * kTile;
             for (int ch = 0; ch < kKChunks && ok; ++ch) {
-              ok = warp_all(wait_bar(s, B_KFULL + g * 9 + ch, (uint32_t)((n >> 1) & 1), p));
+              const long long m = n * kKChunks + ch;
+              const int slot = (int)(m % kKSlots);
+              ok = warp_all(wait_bar(s, B_KFULL + slot, (uint32_t)((m / kKSlots) & 1), p));
               if (!ok) break;
               tc_fence_after();
-              const uint32_t kb = s.base + kOffRing + (g * 9 + ch) * kChunkBytes;
+              const uint32_t kb = s.base + kOffRing + slot * kChunkBytes;
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const uint64_t bdesc = smem_desc(kb + 32 * k, 16, 1024, kSwizzle128B);
@@ -485,9 +500,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 else
                   mma_ss_warp(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128B), bdesc, idesc, 1);
               }
+              mma_commit_warp(bar_addr(s.base, B_KEMPTY + slot));   // this chunk's slot is free
             }
             if (!ok) break;
-            mma_commit_warp(bar_addr(s.base, B_KEMPTY + g));
             mma_commit_warp(bar_addr(s.base, B_SFULL + g));
           }
           if (!ok || !warp_all(*s.abort == 0)) break;
@@ -679,6 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- V producer -----------------------------------------------------------------
       SegIter it;
       long long n = 0;
+      long long issued = 0;     // half-tile groups issued
       if (seg_first(p, c, it, T, s_scan)) {
         do {
           const int b = it.u / p.row_tiles;
@@ -686,30 +702,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int seg_keys = min(keys, it.t_end * kTile);
           const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
           for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
-            const int g = (int)(n & 1);
-            if (!wait_bar(s, B_VEMPTY + g, (uint32_t)(((n >> 1) + 1) & 1), p)) break;
             const int t0 = t * kTile;
-            for (int ch = 0; ch < kVChunks; ++ch) {
-              const uint32_t fb = bar_addr(s.base, B_VFULL + g * 8 + ch);
-              mbar_arrive_expect_tx(fb, kChunkBytes);
-              const uint32_t dst = s.base + kOffRing + (g * 8 + ch) * kChunkBytes;
-              for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
-                const int tok = t0 + r0;
-                int y = p.num_blocks * p.bs;
-                if (tok < seg_keys) {
-                  const int page = __ldg(btrow + tok / p.bs);
-                  if (page >= 0 && page < p.num_blocks) y = page * p.bs + tok % p.bs;
+            bool okv = true;
+            for (int h = 0; h < 2 && okv; ++h) {
+              const long long q = 2 * n + h;                  // half-tile sequence number
+              const int grp = (int)(q % kVGroups);
+              okv = wait_bar(s, B_VEMPTY + grp, (uint32_t)(((q / kVGroups) + 1) & 1), p);
+              if (!okv) break;
+              const uint32_t fb = bar_addr(s.base, B_VFULL + grp);
+              mbar_arrive_expect_tx(fb, 4 * kChunkBytes);
+              for (int ch = 4 * h; ch < 4 * h + 4; ++ch) {
+                const uint32_t dst = s.base + kOffRing + (grp * 4 + (ch - 4 * h)) * kChunkBytes;
+                for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
+                  const int tok = t0 + r0;
+                  int y = p.num_blocks * p.bs;
+                  if (tok < seg_keys) {
+                    const int page = __ldg(btrow + tok / p.bs);
+                    if (page >= 0 && page < p.num_blocks) y = page * p.bs + tok % p.bs;
+                  }
+                  tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
                 }
-                tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
               }
+              issued = q + 1;
             }
+            if (!okv) break;
           }
         } while (!*s.abort && seg_next(p, it));
       }
       if (*s.abort) {
-        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
-          for (int ch = 0; ch < kVChunks; ++ch)
-            mbar_wait_drain(bar_addr(s.base, B_VFULL + (int)(k & 1) * 8 + ch), (uint32_t)((k >> 1) & 1));
+        for (long long q = (issued > kVGroups ? issued - kVGroups : 0); q < issued; ++q)
+          mbar_wait_drain(bar_addr(s.base, B_VFULL + (int)(q % kVGroups)), (uint32_t)((q / kVGroups) & 1));
       }
     } else if (warp == 1) {
       // ---- PV MMA issuer (lane 0 issues; the warp zeroes V rows past the keys) ---------
@@ -729,7 +751,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           bool ok = true;
           for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
-            const int g = (int)(n & 1), j = (int)(n & 1);
+            const int j = (int)(n & 1);
             ok = warp_all(wait_bar(s, B_PFULL + j, (uint32_t)((n >> 1) & 1), p, true));
             if (!ok) break;
             const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
@@ -758,41 +780,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            for (int ch = 0; ch < kVChunks && ok; ++ch)
-              ok = warp_all(wait_bar(s, B_VFULL + g * 8 + ch, (uint32_t)((n >> 1) & 1), p));
-            if (!ok) break;
             const int t0 = t * kTile;
             const int valid_keys = seg_keys - t0;
-            if (valid_keys < kTile) {
-              // zero V rows [valid_keys, 64) of all chunks (whole 128-byte rows)
-              const int r_lo = valid_keys < 0 ? 0 : valid_keys;
-              for (int ch = 0; ch < kVChunks; ++ch) {
-                uint8_t* base = s.ptr + kOffRing + (g * 8 + ch) * kChunkBytes;
-                for (int idx = r_lo * 8 + lane; idx < kTile * 8; idx += 32) {
-                  const int rr = idx >> 3, q = idx & 7;
-                  *reinterpret_cast<uint4*>(base + (rr >> 3) * 1024 + (rr & 7) * 128 + q * 16) =
-                      make_uint4(0, 0, 0, 0);
+            const uint32_t pa = s.base + kOffP + j * kPSlotBytes;
+            for (int h = 0; h < 2 && ok; ++h) {
+              const long long q = 2 * n + h;
+              const int grp = (int)(q % kVGroups);
+              ok = warp_all(wait_bar(s, B_VFULL + grp, (uint32_t)((q / kVGroups) & 1), p));
+              if (!ok) break;
+              if (valid_keys < kTile) {
+                // zero V rows [valid_keys, 64) of the group's 4 chunks (whole 128-byte rows)
+                const int r_lo = valid_keys < 0 ? 0 : valid_keys;
+                for (int cc = 0; cc < 4; ++cc) {
+                  uint8_t* base = s.ptr + kOffRing + (grp * 4 + cc) * kChunkBytes;
+                  for (int idx = r_lo * 8 + lane; idx < kTile * 8; idx += 32) {
+                    const int rr = idx >> 3, qq = idx & 7;
+                    *reinterpret_cast<uint4*>(base + (rr >> 3) * 1024 + (rr & 7) * 128 + qq * 16) =
+                        make_uint4(0, 0, 0, 0);
+                  }
                 }
+                fence_proxy_async_smem();
               }
-              fence_proxy_async_smem();
               __syncwarp();
-            }
-            __syncwarp();
-            tc_fence_after();
-            {
-              const uint32_t pa = s.base + kOffP + j * kPSlotBytes;
-              const uint32_t vb = s.base + kOffRing + g * 8 * kChunkBytes;
+              tc_fence_after();
+              const uint32_t vb = s.base + kOffRing + grp * 4 * kChunkBytes;
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const uint64_t adesc = smem_desc(pa + 32 * k, 16, 1024, kSwizzle128B);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const uint64_t bdesc =
-                      smem_desc(vb + h * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024, kSwizzle128B);
-                  mma_ss_warp(tmem + h * 256, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
-                }
+                const uint64_t bdesc = smem_desc(vb + k * 2048, kChunkBytes, 1024, kSwizzle128B);
+                mma_ss_warp(tmem + h * 256, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
               }
-              mma_commit_warp(bar_addr(s.base, B_VEMPTY + g));
+              mma_commit_warp(bar_addr(s.base, B_VEMPTY + grp));     // this half's group is free
+            }
+            if (!ok) break;
+            {
               mma_commit_multicast_warp(bar_addr(s.base, B_PFREE + j), (uint16_t)1);
               if (last) mma_commit_warp(bar_addr(s.base, B_OFINAL));
             }
