@@ -420,48 +420,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (is_s) {
     // ============================== S-CTA ==========================================
-    if (warp == 0 && lane == 0) {
-      // ---- K producer ---------------------------------------------------------------
+    if (warp == 0) {
+      // ---- K producer (the whole warp runs the loop; one elected lane issues) ----------
       SegIter it;
       long long n = 0;      // global tile counter of this cluster
       long long issued = 0; // key chunks issued
       bool bad = false;
+      int slot = 0;
+      uint32_t par = 1;     // a slot's first use passes at once
+      bool okk = true;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
           const int b = it.u / p.row_tiles;
           const int keys = unit_keys(p, it.u);
           const int seg_keys = min(keys, it.t_end * kTile);
           const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
-          for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
+          const int nbox = kTile / p.box_rows;
+          for (int t = it.t_begin; t < it.t_end && okk; ++t, ++n) {
             const int t0 = t * kTile;
-            bool okk = true;
-            for (int ch = 0; ch < kKChunks && okk; ++ch) {
-              const long long m = n * kKChunks + ch;          // chunk sequence number
-              const int slot = (int)(m % kKSlots);
-              okk = wait_bar(s, B_KEMPTY + slot, (uint32_t)(((m / kKSlots) + 1) & 1), p);
+            // rows of the tile's TMA boxes (one page lookup per box, not per chunk);
+            // a missing or invalid page becomes a row past the cache, which TMA zero-fills
+            int ys[4];
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx) {
+              ys[bx] = p.num_blocks * p.bs;
+              const int tok = t0 + bx * p.box_rows;
+              if (bx < nbox && tok < seg_keys) {
+                const int page = __ldg(btrow + tok / p.bs);
+                if (page >= 0 && page < p.num_blocks)
+                  ys[bx] = page * p.bs + tok % p.bs;
+                else
+                  bad = true;
+              }
+            }
+            for (int ch = 0; ch < kKChunks; ++ch) {
+              okk = warp_all(wait_bar(s, B_KEMPTY + slot, par, p));
               if (!okk) break;
               const uint32_t fb = bar_addr(s.base, B_KFULL + slot);
-              mbar_arrive_expect_tx(fb, kChunkBytes);
+              mbar_arrive_expect_tx_warp(fb, kChunkBytes);
               const uint32_t dst = s.base + kOffRing + slot * kChunkBytes;
-              for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
-                const int tok = t0 + r0;
-                int y = p.num_blocks * p.bs;       // past the cache: zero fill
-                if (tok < seg_keys) {
-                  const int page = __ldg(btrow + tok / p.bs);
-                  if (page >= 0 && page < p.num_blocks)
-                    y = page * p.bs + tok % p.bs;
-                  else
-                    bad = true;
-                }
-                tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
+#pragma unroll
+              for (int bx = 0; bx < 4; ++bx)
+                if (bx < nbox) tma_load_2d_warp(dst + bx * p.box_rows * 128, &kv_map, ch * 64, ys[bx], fb);
+              ++issued;
+              if (++slot == kKSlots) {
+                slot = 0;
+                par ^= 1u;
               }
-              issued = m + 1;
             }
-            if (!okk) break;
           }
-        } while (!*s.abort && seg_next(p, it));
+        } while (okk && warp_all(*s.abort == 0) && seg_next(p, it));
       }
-      if (bad) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+      if (bad && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
       if (*s.abort) {
         // let loads already issued land before the CTA exits
         for (long long m = (issued > kKSlots ? issued - kKSlots : 0); m < issued; ++m)
@@ -485,22 +495,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + 256 + g * kTile;
-            for (int ch = 0; ch < kKChunks && ok; ++ch) {
-              const long long m = n * kKChunks + ch;
-              const int slot = (int)(m % kKSlots);
-              ok = warp_all(wait_bar(s, B_KFULL + slot, (uint32_t)((m / kKSlots) & 1), p));
+            // chunk ch of tile n lives in slot (9n + ch) mod 21; the 32 latent MMAs take A
+            // from TMEM, the 4 rope MMAs from shared memory.  Straight-line issue: a branch
+            // between elect.sync MMAs costs more than the MMA itself.
+            long long m = n * kKChunks;
+            int slot = (int)(m % kKSlots);
+            uint32_t par = (uint32_t)((m / kKSlots) & 1);
+            for (int ch = 0; ch < kKChunks; ++ch) {
+              ok = warp_all(wait_bar(s, B_KFULL + slot, par, p));
               if (!ok) break;
-              tc_fence_after();
-              const uint32_t kb = s.base + kOffRing + slot * kChunkBytes;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t bdesc = smem_desc(kb + 32 * k, 16, 1024, kSwizzle128B);
-                if (ch < 8)
-                  mma_ts_warp(d, tmem + ch * 32 + k * 8, bdesc, idesc, (ch | k) != 0);
-                else
-                  mma_ss_warp(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128B), bdesc, idesc, 1);
+              const uint64_t b0 = smem_desc(s.base + kOffRing + slot * kChunkBytes, 16, 1024,
+                                            kSwizzle128B);
+              if (ch < 8) {
+                const uint32_t a0 = tmem + ch * 32;
+                mma_ts_warp(d, a0, b0, idesc, ch != 0);
+                mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
+                mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
+                mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
+              } else {
+                const uint64_t a0 = smem_desc(qrope, 16, 1024, kSwizzle128B);
+                mma_ss_warp(d, a0, b0, idesc, 1);
+                mma_ss_warp(d, a0 + 2, b0 + 2, idesc, 1);
+                mma_ss_warp(d, a0 + 4, b0 + 4, idesc, 1);
+                mma_ss_warp(d, a0 + 6, b0 + 6, idesc, 1);
               }
               mma_commit_warp(bar_addr(s.base, B_KEMPTY + slot));   // this chunk's slot is free
+              if (++slot == kKSlots) {
+                slot = 0;
+                par ^= 1u;
+              }
             }
             if (!ok) break;
             mma_commit_warp(bar_addr(s.base, B_SFULL + g));
@@ -690,44 +713,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================== O-CTA ==========================================
-    if (warp == 0 && lane == 0) {
-      // ---- V producer -----------------------------------------------------------------
+    if (warp == 0) {
+      // ---- V producer (the whole warp runs the loop; one elected lane issues) ----------
       SegIter it;
       long long n = 0;
       long long issued = 0;     // half-tile groups issued
+      int grp = 0;
+      uint32_t par = 1;
+      bool okv = true;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
           const int b = it.u / p.row_tiles;
           const int keys = unit_keys(p, it.u);
           const int seg_keys = min(keys, it.t_end * kTile);
           const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
-          for (int t = it.t_begin; t < it.t_end && !*s.abort; ++t, ++n) {
+          const int nbox = kTile / p.box_rows;
+          for (int t = it.t_begin; t < it.t_end && okv; ++t, ++n) {
             const int t0 = t * kTile;
-            bool okv = true;
-            for (int h = 0; h < 2 && okv; ++h) {
-              const long long q = 2 * n + h;                  // half-tile sequence number
-              const int grp = (int)(q % kVGroups);
-              okv = wait_bar(s, B_VEMPTY + grp, (uint32_t)(((q / kVGroups) + 1) & 1), p);
+            int ys[4];
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx) {
+              ys[bx] = p.num_blocks * p.bs;
+              const int tok = t0 + bx * p.box_rows;
+              if (bx < nbox && tok < seg_keys) {
+                const int page = __ldg(btrow + tok / p.bs);
+                if (page >= 0 && page < p.num_blocks) ys[bx] = page * p.bs + tok % p.bs;
+              }
+            }
+            for (int h = 0; h < 2; ++h) {
+              okv = warp_all(wait_bar(s, B_VEMPTY + grp, par, p));
               if (!okv) break;
               const uint32_t fb = bar_addr(s.base, B_VFULL + grp);
-              mbar_arrive_expect_tx(fb, 4 * kChunkBytes);
-              for (int ch = 4 * h; ch < 4 * h + 4; ++ch) {
-                const uint32_t dst = s.base + kOffRing + (grp * 4 + (ch - 4 * h)) * kChunkBytes;
-                for (int r0 = 0; r0 < kTile; r0 += p.box_rows) {
-                  const int tok = t0 + r0;
-                  int y = p.num_blocks * p.bs;
-                  if (tok < seg_keys) {
-                    const int page = __ldg(btrow + tok / p.bs);
-                    if (page >= 0 && page < p.num_blocks) y = page * p.bs + tok % p.bs;
-                  }
-                  tma_load_2d(dst + r0 * 128, &kv_map, ch * 64, y, fb);
-                }
+              mbar_arrive_expect_tx_warp(fb, 4 * kChunkBytes);
+              for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t dst = s.base + kOffRing + (grp * 4 + cc) * kChunkBytes;
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx)
+                  if (bx < nbox)
+                    tma_load_2d_warp(dst + bx * p.box_rows * 128, &kv_map, (4 * h + cc) * 64, ys[bx], fb);
               }
-              issued = q + 1;
+              ++issued;
+              if (++grp == kVGroups) {
+                grp = 0;
+                par ^= 1u;
+              }
             }
-            if (!okv) break;
           }
-        } while (!*s.abort && seg_next(p, it));
+        } while (okv && warp_all(*s.abort == 0) && seg_next(p, it));
       }
       if (*s.abort) {
         for (long long q = (issued > kVGroups ? issued - kVGroups : 0); q < issued; ++q)

@@ -366,5 +366,24 @@ __device__ __forceinline__ void mma_commit_multicast_warp(uint32_t bar, uint16_t
       : "memory");
 }
 
+// Warp-collective TMA issue and expect_tx (converged warp, one elected lane acts).
+__device__ __forceinline__ void tma_load_2d_warp(uint32_t smem_dst, const CUtensorMap* map, int x,
+                                                 int y, uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3}], [%4];\n}" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
 }  // namespace sm100
 }  // namespace mla
