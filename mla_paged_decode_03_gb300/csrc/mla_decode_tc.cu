@@ -60,7 +60,8 @@ constexpr int kM = 128;             // query rows per unit
 constexpr int kTile = 64;           // keys per tile
 constexpr int kChunkBytes = kTile * 128;      // 64 keys x 64 dims bf16 = 8 KB
 constexpr int kKChunks = 9;         // 8 latent + 1 rope chunks per tile (S-CTA)
-constexpr int kKSlots = 21;         // S-CTA key ring: 21 chunk slots (2.33 tiles), freed per chunk
+constexpr int kKGroup = 3;          // key chunks per TMA group (one 3-D box)
+constexpr int kKGroups = 7;         // S-CTA key ring: 7 slots of 3 chunks (2.33 tiles)
 constexpr int kVGroups = 5;         // O-CTA value ring: 5 half-tile groups of 4 chunks (2.5 tiles)
 constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
 constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
@@ -71,8 +72,8 @@ constexpr int kEvCorrect = 1;
 constexpr int kEvFinal = 2;
 
 // shared memory layout (identical offsets in both CTAs of a pair)
-constexpr int kOffRing = 0;                                  // 21 x 8 KB (S) / 5 x 32 KB (O)
-constexpr int kOffQRope = kOffRing + kKSlots * kChunkBytes;  // 172032
+constexpr int kOffRing = 0;                                  // 7 x 24 KB (S) / 5 x 32 KB (O)
+constexpr int kOffQRope = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032
 constexpr int kOffP = kOffQRope + kM * 128;                  // 188416
 constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 225280
 constexpr int kOffFinInvL = kOffBar + 1024;                  // 128 floats (O-CTA)
@@ -82,23 +83,23 @@ constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slac
 // barrier indices (8 bytes each) inside [kOffBar, kOffBar + 1024)
 enum Bar : int {
   // S-CTA
-  B_KFULL = 0,            // [21] per key chunk slot
-  B_KEMPTY = 21,          // [21]
-  B_SFULL = 42,           // [2]
-  B_SFREE = 44,           // [2]
-  B_QREADY = 46,
-  B_QFREE = 47,
-  B_PFREE = 48,           // [2]  (arrived by the O-CTA's multicast commit)
+  B_KFULL = 0,            // [7] per key group slot
+  B_KEMPTY = 7,           // [7]
+  B_SFULL = 14,           // [2]
+  B_SFREE = 16,           // [2]
+  B_QREADY = 18,
+  B_QFREE = 19,
+  B_PFREE = 20,           // [2]  (arrived by the O-CTA's multicast commit)
   // O-CTA
-  B_VFULL = 50,           // [5] per half-tile value group
-  B_VEMPTY = 55,          // [5]
-  B_PFULL = 60,           // [2]  (completed by the S-CTA's bulk copy)
-  B_PVDONE = 62,
-  B_EV = 63,              // MMA warp -> correction warps: one event (rescale or final)
-  B_CORRDONE = 64,
-  B_OFINAL = 65,
-  B_OFREE = 66,
-  B_COUNT = 67
+  B_VFULL = 22,           // [5] per half-tile value group
+  B_VEMPTY = 27,          // [5]
+  B_PFULL = 32,           // [2]  (completed by the S-CTA's bulk copy)
+  B_PVDONE = 34,
+  B_EV = 35,              // MMA warp -> correction warps: one event (rescale or final)
+  B_CORRDONE = 36,
+  B_OFINAL = 37,
+  B_OFREE = 38,
+  B_COUNT = 39
 };
 
 struct Params {
@@ -114,6 +115,7 @@ struct Params {
   int clusters;        // C
   int whole_units;     // 1: no workspace, each cluster takes whole units round-robin
   int box_rows;        // rows per TMA box = min(bs, 64)
+  int kz, vz;          // chunks per K / V TMA box (3 and 4, or 1 when a page is < 64 rows)
   float scale_log2;
   float lse_mul;
   uint16_t* out;
@@ -179,6 +181,48 @@ __device__ __forceinline__ long long range_start(long long T, int c, int C) {
 __device__ __forceinline__ int owner_of(long long x, long long T, int C) {
   return (int)(((x + 1) * C - 1) / T);
 }
+
+// Cache rows of a segment's TMA boxes for a producer warp: box i covers box_rows keys
+// from token i * box_rows; a missing or invalid page becomes a row past the cache, which
+// TMA fills with zeros.  Lane l holds box i0 + l of the current window of 32 boxes, and the
+// page numbers of the next window are loaded one window ahead.
+struct BoxWindow {
+  const int32_t* btrow;
+  int seg_keys, i0, cur, nxt, lane;
+  bool bad;
+
+  __device__ int row_of(const Params& p, int i) {
+    const int tok = i * p.box_rows;
+    int y = p.num_blocks * p.bs;
+    if (tok < seg_keys) {
+      const int page = __ldg(btrow + tok / p.bs);
+      if (page >= 0 && page < p.num_blocks)
+        y = page * p.bs + tok % p.bs;
+      else
+        bad = true;
+    }
+    return y;
+  }
+  __device__ void start(const Params& p, const SegIter& it) {
+    btrow = p.bt + (long long)(it.u / p.row_tiles) * p.bt_stride;
+    seg_keys = min(unit_keys(p, it.u), it.t_end * kTile);
+    i0 = it.t_begin * (kTile / p.box_rows);
+    cur = row_of(p, i0 + lane);
+    nxt = row_of(p, i0 + 32 + lane);
+  }
+  // rows of the boxes of tile t; warp-collective.  A tile's boxes (1, 2 or 4 of them)
+  // never straddle two windows.
+  __device__ void tile_rows(const Params& p, int t, int (&ys)[4]) {
+    const int nbox = kTile / p.box_rows;
+    if (t * nbox >= i0 + 32) {
+      i0 += 32;
+      cur = nxt;
+      nxt = row_of(p, i0 + 32 + lane);
+    }
+#pragma unroll
+    for (int bx = 0; bx < 4; ++bx) ys[bx] = __shfl_sync(0xffffffffu, cur, (t * nbox + bx - i0) & 31);
+  }
+};
 
 // ---------------------------------------------------------------------------------
 // kernel
@@ -299,7 +343,8 @@ __device__ bool seg_next(const Params& p, SegIter& it) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const Params p) {
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SmemCtx s;
   s.ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -317,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup: barriers, TMEM, schedule scan -----------------------------------------
   if (tid == 0) {
     *s.abort = 0;
-    for (int i = 0; i < kKSlots; ++i) {
+    for (int i = 0; i < kKGroups; ++i) {
       mbar_init(bar_addr(s.base, B_KFULL + i), 1);
       mbar_init(bar_addr(s.base, B_KEMPTY + i), 1);
     }
@@ -421,49 +466,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (is_s) {
     // ============================== S-CTA ==========================================
     if (warp == 0) {
-      // ---- K producer (the whole warp runs the loop; one elected lane issues) ----------
+      // ---- K producer: per tile 3 groups of 3 chunks, each one 3-D TMA box per page
+      // part (the whole warp runs the loop; one elected lane issues) --------------------
+      if (lane == 0) prefetch_tensormap(&kmap);
       SegIter it;
-      long long n = 0;      // global tile counter of this cluster
-      long long issued = 0; // key chunks issued
-      bool bad = false;
+      BoxWindow win;
+      win.lane = lane;
+      win.bad = false;
+      long long issued = 0; // key groups issued
       int slot = 0;
       uint32_t par = 1;     // a slot's first use passes at once
       bool okk = true;
+      const int nbox = kTile / p.box_rows;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
-          const int b = it.u / p.row_tiles;
-          const int keys = unit_keys(p, it.u);
-          const int seg_keys = min(keys, it.t_end * kTile);
-          const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
-          const int nbox = kTile / p.box_rows;
-          for (int t = it.t_begin; t < it.t_end && okk; ++t, ++n) {
-            const int t0 = t * kTile;
-            // rows of the tile's TMA boxes (one page lookup per box, not per chunk);
-            // a missing or invalid page becomes a row past the cache, which TMA zero-fills
+          win.start(p, it);
+          for (int t = it.t_begin; t < it.t_end && okk; ++t) {
             int ys[4];
-#pragma unroll
-            for (int bx = 0; bx < 4; ++bx) {
-              ys[bx] = p.num_blocks * p.bs;
-              const int tok = t0 + bx * p.box_rows;
-              if (bx < nbox && tok < seg_keys) {
-                const int page = __ldg(btrow + tok / p.bs);
-                if (page >= 0 && page < p.num_blocks)
-                  ys[bx] = page * p.bs + tok % p.bs;
-                else
-                  bad = true;
-              }
-            }
-            for (int ch = 0; ch < kKChunks; ++ch) {
+            win.tile_rows(p, t, ys);
+            for (int g = 0; g < kKChunks / kKGroup; ++g) {
               okk = warp_all(wait_bar(s, B_KEMPTY + slot, par, p));
               if (!okk) break;
               const uint32_t fb = bar_addr(s.base, B_KFULL + slot);
-              mbar_arrive_expect_tx_warp(fb, kChunkBytes);
-              const uint32_t dst = s.base + kOffRing + slot * kChunkBytes;
+              mbar_arrive_expect_tx_warp(fb, kKGroup * kChunkBytes);
+              const uint32_t dst = s.base + kOffRing + slot * kKGroup * kChunkBytes;
+              for (int cc = 0; cc < kKGroup; cc += p.kz)
 #pragma unroll
-              for (int bx = 0; bx < 4; ++bx)
-                if (bx < nbox) tma_load_2d_warp(dst + bx * p.box_rows * 128, &kv_map, ch * 64, ys[bx], fb);
+                for (int bx = 0; bx < 4; ++bx)
+                  if (bx < nbox)
+                    tma_load_3d_warp(dst + cc * kChunkBytes + bx * p.box_rows * 128, &kmap, 0, ys[bx],
+                                     kKGroup * g + cc, fb);
               ++issued;
-              if (++slot == kKSlots) {
+              if (++slot == kKGroups) {
                 slot = 0;
                 par ^= 1u;
               }
@@ -471,11 +505,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         } while (okk && warp_all(*s.abort == 0) && seg_next(p, it));
       }
-      if (bad && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
-      if (*s.abort) {
+      if (__any_sync(0xffffffffu, win.bad) && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+      if (*s.abort && lane == 0) {
         // let loads already issued land before the CTA exits
-        for (long long m = (issued > kKSlots ? issued - kKSlots : 0); m < issued; ++m)
-          mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(m % kKSlots)), (uint32_t)((m / kKSlots) & 1));
+        for (long long m = (issued > kKGroups ? issued - kKGroups : 0); m < issued; ++m)
+          mbar_wait_drain(bar_addr(s.base, B_KFULL + (int)(m % kKGroups)), (uint32_t)((m / kKGroups) & 1));
       }
     } else if (warp == 1) {
       // ---- QK MMA issuer (the whole warp runs the loop; one elected lane issues) --------
@@ -484,6 +518,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int nseg = 0;
       const uint32_t idesc = idesc_bf16(kM, kTile, false, false);
       const uint32_t qrope = s.base + kOffQRope;
+      int kslot = 0;          // key group slot of the next group, and its phase parity
+      uint32_t kpar = 0;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
           if (!warp_all(wait_bar(s, B_QREADY, (uint32_t)(nseg & 1), p))) break;
@@ -495,34 +531,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + 256 + g * kTile;
-            // chunk ch of tile n lives in slot (9n + ch) mod 21; the 32 latent MMAs take A
-            // from TMEM, the 4 rope MMAs from shared memory.  Straight-line issue: a branch
-            // between elect.sync MMAs costs more than the MMA itself.
-            long long m = n * kKChunks;
-            int slot = (int)(m % kKSlots);
-            uint32_t par = (uint32_t)((m / kKSlots) & 1);
-            for (int ch = 0; ch < kKChunks; ++ch) {
-              ok = warp_all(wait_bar(s, B_KFULL + slot, par, p));
+            // the tile's chunks arrive in 3 groups (slots 3n .. 3n+2 mod 7); the 32 latent
+            // MMAs take A from TMEM, the 4 rope MMAs from shared memory.  The loops are
+            // unrolled so that the issue sequence has no branch between MMAs.
+#pragma unroll
+            for (int gi = 0; gi < kKChunks / kKGroup; ++gi) {
+              ok = warp_all(wait_bar(s, B_KFULL + kslot, kpar, p));
               if (!ok) break;
-              const uint64_t b0 = smem_desc(s.base + kOffRing + slot * kChunkBytes, 16, 1024,
-                                            kSwizzle128B);
-              if (ch < 8) {
-                const uint32_t a0 = tmem + ch * 32;
-                mma_ts_warp(d, a0, b0, idesc, ch != 0);
-                mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
-                mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
-                mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
-              } else {
-                const uint64_t a0 = smem_desc(qrope, 16, 1024, kSwizzle128B);
-                mma_ss_warp(d, a0, b0, idesc, 1);
-                mma_ss_warp(d, a0 + 2, b0 + 2, idesc, 1);
-                mma_ss_warp(d, a0 + 4, b0 + 4, idesc, 1);
-                mma_ss_warp(d, a0 + 6, b0 + 6, idesc, 1);
+              const uint32_t gb = s.base + kOffRing + kslot * kKGroup * kChunkBytes;
+#pragma unroll
+              for (int cc = 0; cc < kKGroup; ++cc) {
+                const int ch = kKGroup * gi + cc;
+                const uint64_t b0 = smem_desc(gb + cc * kChunkBytes, 16, 1024, kSwizzle128B);
+                if (ch < 8) {
+                  const uint32_t a0 = tmem + ch * 32;
+                  mma_ts_warp(d, a0, b0, idesc, ch != 0);
+                  mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
+                  mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
+                  mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
+                } else {
+                  const uint64_t a0 = smem_desc(qrope, 16, 1024, kSwizzle128B);
+                  mma_ss_warp(d, a0, b0, idesc, 1);
+                  mma_ss_warp(d, a0 + 2, b0 + 2, idesc, 1);
+                  mma_ss_warp(d, a0 + 4, b0 + 4, idesc, 1);
+                  mma_ss_warp(d, a0 + 6, b0 + 6, idesc, 1);
+                }
               }
-              mma_commit_warp(bar_addr(s.base, B_KEMPTY + slot));   // this chunk's slot is free
-              if (++slot == kKSlots) {
-                slot = 0;
-                par ^= 1u;
+              mma_commit_warp(bar_addr(s.base, B_KEMPTY + kslot));   // this group's slot is free
+              if (++kslot == kKGroups) {
+                kslot = 0;
+                kpar ^= 1u;
               }
             }
             if (!ok) break;
@@ -714,44 +752,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ============================== O-CTA ==========================================
     if (warp == 0) {
-      // ---- V producer (the whole warp runs the loop; one elected lane issues) ----------
+      // ---- V producer: per half tile one group of 4 chunks, one 3-D TMA box per page
+      // part (the whole warp runs the loop; one elected lane issues) --------------------
+      if (lane == 0) prefetch_tensormap(&vmap);
       SegIter it;
-      long long n = 0;
+      BoxWindow win;
+      win.lane = lane;
+      win.bad = false;
       long long issued = 0;     // half-tile groups issued
       int grp = 0;
       uint32_t par = 1;
       bool okv = true;
+      const int nbox = kTile / p.box_rows;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
-          const int b = it.u / p.row_tiles;
-          const int keys = unit_keys(p, it.u);
-          const int seg_keys = min(keys, it.t_end * kTile);
-          const int32_t* btrow = p.bt + (long long)b * p.bt_stride;
-          const int nbox = kTile / p.box_rows;
-          for (int t = it.t_begin; t < it.t_end && okv; ++t, ++n) {
-            const int t0 = t * kTile;
+          win.start(p, it);
+          for (int t = it.t_begin; t < it.t_end && okv; ++t) {
             int ys[4];
-#pragma unroll
-            for (int bx = 0; bx < 4; ++bx) {
-              ys[bx] = p.num_blocks * p.bs;
-              const int tok = t0 + bx * p.box_rows;
-              if (bx < nbox && tok < seg_keys) {
-                const int page = __ldg(btrow + tok / p.bs);
-                if (page >= 0 && page < p.num_blocks) ys[bx] = page * p.bs + tok % p.bs;
-              }
-            }
+            win.tile_rows(p, t, ys);
             for (int h = 0; h < 2; ++h) {
               okv = warp_all(wait_bar(s, B_VEMPTY + grp, par, p));
               if (!okv) break;
               const uint32_t fb = bar_addr(s.base, B_VFULL + grp);
               mbar_arrive_expect_tx_warp(fb, 4 * kChunkBytes);
-              for (int cc = 0; cc < 4; ++cc) {
-                const uint32_t dst = s.base + kOffRing + (grp * 4 + cc) * kChunkBytes;
+              const uint32_t dst = s.base + kOffRing + grp * 4 * kChunkBytes;
+              for (int cc = 0; cc < 4; cc += p.vz)
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx)
                   if (bx < nbox)
-                    tma_load_2d_warp(dst + bx * p.box_rows * 128, &kv_map, (4 * h + cc) * 64, ys[bx], fb);
-              }
+                    tma_load_3d_warp(dst + cc * kChunkBytes + bx * p.box_rows * 128, &vmap, 0, ys[bx],
+                                     4 * h + cc, fb);
               ++issued;
               if (++grp == kVGroups) {
                 grp = 0;
@@ -761,7 +791,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         } while (okv && warp_all(*s.abort == 0) && seg_next(p, it));
       }
-      if (*s.abort) {
+      if (*s.abort && lane == 0) {
         for (long long q = (issued > kVGroups ? issued - kVGroups : 0); q < issued; ++q)
           mbar_wait_drain(bar_addr(s.base, B_VFULL + (int)(q % kVGroups)), (uint32_t)((q / kVGroups) & 1));
       }
@@ -1150,20 +1180,32 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     p.clusters = C;
   }
 
-  CUtensorMap map;
+  // The cache seen as [rows][9 chunks][64 dims]: dims 64 elements (contiguous), rows
+  // (stride 1152 bytes), chunks (stride 128 bytes).  One box takes box_rows keys of
+  // kz (vz) consecutive chunks and lands as [chunk][key][128 bytes], 128-byte swizzled,
+  // which is the MMA operand layout of each chunk.
+  CUtensorMap kmap, vmap;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.num_blocks * a.block_size};
-    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = get_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                               const_cast<uint16_t*>(a.kv), dims, strides, box, es,
+    p.kz = p.box_rows == 64 ? kKGroup : 1;
+    p.vz = p.box_rows == 64 ? 4 : 1;
+    cuuint64_t dims[3] = {64, (cuuint64_t)a.num_blocks * a.block_size, (cuuint64_t)kKChunks};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    cuuint32_t kbox[3] = {64, (cuuint32_t)p.box_rows, (cuuint32_t)p.kz};
+    cuuint32_t vbox[3] = {64, (cuuint32_t)p.box_rows, (cuuint32_t)p.vz};
+    CUresult r = get_encoder()(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                               const_cast<uint16_t*>(a.kv), dims, strides, kbox, es,
                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    r = get_encoder()(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.kv),
+                      dims, strides, vbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(map, p);
+  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = (long long)p.units * kM;

@@ -166,6 +166,19 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// 16-byte store into shared::cluster memory (normally a peer CTA's) that completes 16
+// bytes of transaction count on the mbarrier at shared::cluster address `cluster_bar`
+// (in the same CTA as the destination).  The receiver learns of the data only through
+// that mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------
 // TMA and bulk copies
 // ---------------------------------------------------------------------------------
@@ -374,6 +387,17 @@ __device__ __forceinline__ void tma_load_2d_warp(uint32_t smem_dst, const CUtens
       " @e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
       "[%1, {%2, %3}], [%4];\n}" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 3-D tile load (coordinates x, y, z), warp-collective like tma_load_2d_warp.
+__device__ __forceinline__ void tma_load_3d_warp(uint32_t smem_dst, const CUtensorMap* map, int x,
+                                                 int y, int z, uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4}], [%5];\n}" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
