@@ -66,6 +66,7 @@ constexpr int kVGroups = 5;         // O-CTA value ring: 5 half-tile groups of 4
 constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
 constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
 constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
+constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages in 2)
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr int kThreads = 256;
 constexpr int kEvCorrect = 1;
@@ -76,6 +77,8 @@ constexpr int kOffRing = 0;                                  // 7 x 24 KB (S) / 
 constexpr int kOffQRope = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032
 constexpr int kOffP = kOffQRope + kM * 128;                  // 188416
 constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 225280
+constexpr int kOffPR = kVGroups * 4 * kChunkBytes;           // 163840: O-CTA receive slots
+static_assert(kOffPR + kPRecv * kPSlotBytes <= kOffBar, "O-CTA receive slots");
 constexpr int kOffFinInvL = kOffBar + 1024;                  // 128 floats (O-CTA)
 constexpr int kOffMisc = kOffFinInvL + 512;                  // tmem base, abort, etc.
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slack
@@ -89,17 +92,20 @@ enum Bar : int {
   B_SFREE = 16,           // [2]
   B_QREADY = 18,
   B_QFREE = 19,
-  B_PFREE = 20,           // [2]  (arrived by the O-CTA's multicast commit)
+  B_PFREE = 20,           // [3]  (arrived by the O-CTA's multicast commit)
   // O-CTA
-  B_VFULL = 22,           // [5] per half-tile value group
-  B_VEMPTY = 27,          // [5]
-  B_PFULL = 32,           // [2]  (completed by the S-CTA's bulk copy)
-  B_PVDONE = 34,
-  B_EV = 35,              // MMA warp -> correction warps: one event (rescale or final)
-  B_CORRDONE = 36,
-  B_OFINAL = 37,
-  B_OFREE = 38,
-  B_COUNT = 39
+  B_VFULL = 23,           // [5] per half-tile value group
+  B_VEMPTY = 28,          // [5]
+  B_PFULL = 33,           // [3]  (completed by the S-CTA's bulk copy)
+  B_PVDONE = 36,
+  B_EV = 37,              // MMA warp -> correction warps: one event (rescale or final)
+  B_CORRDONE = 38,
+  B_OFINAL = 39,
+  B_OFREE = 40,
+  // S-CTA: softmax warps <-> copy warp
+  B_PSTAGED = 41,         // [2] P + sideband written into a staging slot (4 warps)
+  B_STAGEFREE = 43,       // [2] the bulk copy has read the staging slot
+  B_COUNT = 45
 };
 
 struct Params {
@@ -373,8 +379,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(s.base, B_SFULL + i), 1);
       mbar_init(bar_addr(s.base, B_SFREE + i), 4);
+    }
+    for (int i = 0; i < kPRecv; ++i) {
       mbar_init(bar_addr(s.base, B_PFREE + i), 1);
       mbar_init(bar_addr(s.base, B_PFULL + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_addr(s.base, B_PSTAGED + i), 4);
+      mbar_init(bar_addr(s.base, B_STAGEFREE + i), 1);
     }
     mbar_init(bar_addr(s.base, B_QREADY), 4);
     mbar_init(bar_addr(s.base, B_QFREE), 1);
@@ -571,11 +583,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++nseg;
         } while (seg_next(p, it));
       }
+    } else if (warp == 2) {
+      // ---- copy warp: each staged P tile (+ sideband) into the O-CTA's receive slot -----
+      // n % 3 once its previous tile there has been multiplied (the O-CTA's commit arrives
+      // on p_free), then the staging slot is handed back to the softmax warps.
+      SegIter it;
+      long long n = 0;
+      bool ok = true;
+      if (lane == 0 && seg_first(p, c, it, T, s_scan)) {
+        do {
+          for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
+            const int j = (int)(n & 1);
+            const int jr = (int)(n % kPRecv);
+            ok = wait_bar(s, B_PSTAGED + j, (uint32_t)((n >> 1) & 1), p) &&
+                 wait_bar(s, B_PFREE + jr, (uint32_t)(((n / kPRecv) & 1) ^ 1), p, true);
+            if (!ok) break;
+            const uint32_t rbar = mapa(bar_addr(s.base, B_PFULL + jr), peer);
+            mbar_arrive_expect_tx_cluster(rbar, kPBytes + kSideBytes);
+            bulk_s2cluster(mapa(s.base + kOffPR + jr * kPSlotBytes, peer),
+                           s.base + kOffP + j * kPSlotBytes, kPBytes + kSideBytes, rbar);
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(bar_addr(s.base, B_STAGEFREE + j));
+          }
+        } while (ok && *s.abort == 0 && seg_next(p, it));
+        bulk_wait<0>();
+        // the O-CTA's last PV commits arrive on this CTA's p_free barriers
+        if (n > 0 && !*s.abort) {
+          for (long long k = (n >= kPRecv ? n - kPRecv : 0); k < n; ++k)
+            wait_bar(s, B_PFREE + (int)(k % kPRecv), (uint32_t)((k / kPRecv) & 1), p, true);
+        }
+      }
     } else if (warp >= 4) {
       // ---- softmax warps: thread = query row -----------------------------------------
       const int r = tid - 128;                      // row within the unit, = TMEM lane
       const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-      const bool leader = (r == 0);
       SegIter it;
       long long n = 0;
       int nseg = 0;
@@ -624,7 +666,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bool aborted = false;
           for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
             const int g = (int)(n & 1);
-            const int j = (int)(n & 1);            // P slot
+            const int j = (int)(n & 1);            // P staging slot
             if (!group_all(wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p))) {
               aborted = true;
               break;
@@ -701,9 +743,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool last = (t + 1 == it.t_end);
             const bool any_resc = __any_sync(0xffffffffu, resc);
 
-            // staging slot j must no longer be read by the bulk copy issued two tiles ago
-            if (leader) bulk_wait_read<1>();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // staging slot j must no longer be read by the copy of tile n-2
+            if (!warp_all(wait_bar(s, B_STAGEFREE + j, (uint32_t)(((n >> 1) & 1) ^ 1), p))) {
+              aborted = true;
+              break;
+            }
             uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
             uint8_t* prow = slot + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -716,18 +760,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
             if (lane == 0) flags[warp - 4] = any_resc ? 1 : 0;
             fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (leader) {
-              if (!wait_bar(s, B_PFREE + j, (uint32_t)(((n >> 1) + 1) & 1), p, true)) {
-                set_abort_both(s, peer);
-              } else {
-                const uint32_t rbar = mapa(bar_addr(s.base, B_PFULL + j), peer);
-                mbar_arrive_expect_tx_cluster(rbar, kPBytes + kSideBytes);
-                bulk_s2cluster(mapa(s.base + kOffP + j * kPSlotBytes, peer),
-                               s.base + kOffP + j * kPSlotBytes, kPBytes + kSideBytes, rbar);
-                bulk_commit();
-              }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(s.base, B_PSTAGED + j));
             if (last && valid) {
               const float lse2 = l > 0.f ? m_ref + log2f(l) : kNegInf;
               const long long grow = (long long)b * p.rows + row;
@@ -741,12 +775,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (aborted || !group_all(*s.abort == 0)) break;
           ++nseg;
         } while (seg_next(p, it));
-      }
-      if (leader) bulk_wait<0>();
-      // drain: the O-CTA's last two PV commits arrive on this CTA's p_free barriers
-      if (leader && n > 0 && !*s.abort) {
-        for (long long k = (n >= 2 ? n - 2 : 0); k < n; ++k)
-          wait_bar(s, B_PFREE + (int)(k & 1), (uint32_t)((k >> 1) & 1), p, true);
       }
     }
   } else {
@@ -813,10 +841,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           bool ok = true;
           for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
-            const int j = (int)(n & 1);
-            ok = warp_all(wait_bar(s, B_PFULL + j, (uint32_t)((n >> 1) & 1), p, true));
+            const int j = (int)(n % kPRecv);       // receive slot of this tile's P
+            ok = warp_all(wait_bar(s, B_PFULL + j, (uint32_t)((n / kPRecv) & 1), p, true));
             if (!ok) break;
-            const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
+            const uint8_t* slot = s.ptr + kOffPR + j * kPSlotBytes;
             const int* flags = reinterpret_cast<const int*>(slot + kPBytes + 1024);
             const bool first = (t == it.t_begin);
             const bool last = (t + 1 == it.t_end);
@@ -844,7 +872,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const int t0 = t * kTile;
             const int valid_keys = seg_keys - t0;
-            const uint32_t pa = s.base + kOffP + j * kPSlotBytes;
+            const uint32_t pa = s.base + kOffPR + j * kPSlotBytes;
             for (int h = 0; h < 2 && ok; ++h) {
               const long long q = 2 * n + h;
               const int grp = (int)(q % kVGroups);
@@ -916,8 +944,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const int ev = *ev_word;
             if ((ev & 0xff) == kEvFinal) break;
-            const int j = (ev >> 8) & 1;
-            const uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
+            const int j = (ev >> 8) & 3;
+            const uint8_t* slot = s.ptr + kOffPR + j * kPSlotBytes;
             tc_fence_after();
             const float a = reinterpret_cast<const float*>(slot + kPBytes)[r];
             if (__any_sync(0xffffffffu, a != 1.f)) {
