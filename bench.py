@@ -19,6 +19,7 @@ independent replica on its own GPU (weak scaling; the step has no cross-GPU exch
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -239,6 +240,28 @@ def time_e2e(step, steps, warmup, flush):
     return dict(ms=statistics.mean(times), h2d=h2d, d2h=d2h)
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum under ncu) of one mla_decode
+# call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
+# source they were taken on: a changed kernel reports null until it is captured again.
+TRAFFIC = {
+    # commit a338e17: decode 21,960,021 + 7,595 B, combine 23,132,501 B (mean of 3 calls)
+    ("cp2", "787006f050d6acc14cded71ef1496a5cf13aa6be04f2d71ef575f0a885a33bdf"): 45100117,
+}
+
+
+def measured_traffic(config, batch):
+    if batch is not None:
+        return None
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                       "mla_paged_decode_03_gb300", "csrc", "mla_decode_tc.cu")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return TRAFFIC.get((config, digest))
+
+
 def summarize(res, pk):
     wk = res["work"]
     ms = statistics.mean(res["step_ms"])
@@ -360,7 +383,8 @@ def run_ours(args):
     else:
         roof = {"bound": "hbm", "achieved": s["decode_call_gbs"], "peak": pk["hbm"],
                 "unit": "GB/s", "frac": s["decode_call_gbs"] / pk["hbm"]}
-    roof.update({"traffic": None, "kernel": "mla_decode call (split-KV decode + split combine)",
+    roof.update({"traffic": measured_traffic(args.config, args.batch),
+                 "kernel": "mla_decode call (split-KV decode + split combine)",
                  "peak_source": pk["source"] + " (burst)"})
     cpu = (cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline
                                                   and args.batch is None) else None)
