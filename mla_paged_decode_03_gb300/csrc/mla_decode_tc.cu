@@ -14,17 +14,19 @@
 //
 //   CTA 0 (the S-CTA) keeps Q's 512 latent dims in TMEM as the A operand (256 columns),
 //     Q's 64 rope dims in shared memory, and two 64-column S buffers.  A TMA warp streams
-//     the keys (9 chunks of 64 keys x 64 dims per tile, 128-byte swizzle) through a ring
-//     of 21 chunk slots, each freed as soon as its MMAs complete; the MMA warp issues 36
-//     MMAs (M=128, N=64, K=16) per tile into S; four softmax warps (one query row per
-//     thread) read S, apply the per-row causal bound, keep the running max / sum (online
-//     softmax in base 2, the running max only moved when a tile's max exceeds it by more
-//     than 2^8), write P (bf16) into a swizzled shared-memory tile and bulk-copy it, with
-//     the per-row rescale factors, into CTA 1.
+//     the keys (9 chunks of 64 keys x 64 dims per tile, 128-byte swizzle, one 3-D box per
+//     3 chunks) through a ring of 7 three-chunk slots, each freed as soon as its MMAs
+//     complete; the MMA warp issues 36 MMAs (M=128, N=64, K=16) per tile into S; four
+//     softmax warps (one query row per thread) read S, apply the per-row causal bound,
+//     keep the running max / sum (online softmax in base 2 against a per-row reference
+//     max, set 2^64 above a tile's max and moved only when a tile's max exceeds it by more
+//     than 2^32, so that P <= 2^32 and rescales of O are rare even when a few keys score
+//     far above the rest), and write P (bf16) with the per-row rescale factors into a
+//     staging slot, which a copy warp bulk-copies into one of three receive slots of CTA 1.
 //   CTA 1 (the O-CTA) holds O in all 512 TMEM columns.  A TMA warp streams the same keys'
 //     first 512 dims (V) through five half-tile groups; the MMA warp issues 8 MMAs (M=128,
-//     N=256, K=16) of P V per tile; four warps rescale O in TMEM on the rare tiles where
-//     the running max moved, and at the end of a segment read O out, scale by 1/l and
+//     N=256, K=16) of P V per tile; four warps rescale O in TMEM on the tiles where the
+//     reference max moved, and at the end of a segment read O out, scale by 1/l and
 //     store it.
 //   Both MMA warps run their loops as whole converged warps and issue through elect.sync.
 //
@@ -67,7 +69,8 @@ constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
 constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
 constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
 constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages in 2)
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr float kRescaleThreshold = 32.0f;    // log2 units: P <= 2^32
+constexpr float kMaxHeadroom = 64.0f;         // reference max set this far above a tile max
 constexpr int kThreads = 256;
 constexpr int kEvCorrect = 1;
 constexpr int kEvFinal = 2;
@@ -252,7 +255,7 @@ __device__ __forceinline__ bool wait_bar(const SmemCtx& s, int i, uint32_t parit
   return false;
 }
 
-// 2^x on the SFU (ex2.approx, flush-to-zero); arguments here are <= 2^8 or -inf.
+// 2^x on the SFU (ex2.approx, flush-to-zero); arguments here are <= 32 or -inf.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -706,12 +709,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float alpha = 1.f;
             bool resc = false;
             if (tmax > m_ref + kRescaleThreshold) {
+              const float m_new = tmax + kMaxHeadroom;
               if (m_ref != kNegInf) {
-                alpha = fast_exp2(m_ref - tmax);
+                alpha = fast_exp2(m_ref - m_new);
                 resc = true;
               }
               l *= alpha;
-              m_ref = tmax;
+              m_ref = m_new;
             }
             const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
             float sum8[8];
