@@ -136,6 +136,13 @@ struct Params {
   unsigned int* status;
 };
 
+// 32-byte global store (one full sector per thread); `dst` 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t bar_addr(uint32_t smem_base, int i) {
   return smem_base + kOffBar + 8 * i;
 }
@@ -978,28 +985,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + lane_off + c32 * 32, v);
             tmem_wait_ld();
             if (!valid) continue;
+            // one row per thread: 32-byte stores write whole sectors
             if (it.single) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)b * p.rows + row) * kDv +
-                                                    c32 * 32);
+              uint16_t* dst = p.out + ((long long)b * p.rows + row) * kDv + c32 * 32;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t w[4];
+              for (int q = 0; q < 2; ++q) {
+                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
-                                                           __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
-                  w[e] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 8; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]) * inv,
+                                     __uint_as_float(v[16 * q + 2 * e + 1]) * inv);
+                st_global_v8(dst + 16 * q, w);
               }
             } else {
-              float4* dst = reinterpret_cast<float4*>(p.ws_o + ((long long)it.slot * kM + r) * kDv +
-                                                      c32 * 32);
+              float* dst = p.ws_o + ((long long)it.slot * kM + r) * kDv + c32 * 32;
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                     __uint_as_float(v[4 * q + 2]) * inv,
-                                     __uint_as_float(v[4 * q + 3]) * inv);
+              for (int q = 0; q < 4; ++q) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[8 * q + e]) * inv);
+                st_global_v8(dst + 8 * q, w);
+              }
             }
           }
           tc_fence_before();
