@@ -125,6 +125,7 @@ struct Params {
   int whole_units;     // 1: no workspace, each cluster takes whole units round-robin
   int box_rows;        // rows per TMA box = min(bs, 64)
   int kz, vz;          // chunks per K / V TMA box (3 and 4, or 1 when a page is < 64 rows)
+  int q_v8, out_v8;    // q / out are 32-byte aligned: rows are read / written in 32-byte pieces
   float scale_log2;
   float lse_mul;
   uint16_t* out;
@@ -135,6 +136,14 @@ struct Params {
   float* ws_o;         // [units + C][128][512]
   unsigned int* status;
 };
+
+// 32-byte read-only global load (one full sector per thread); `src` 32-byte aligned.
+__device__ __forceinline__ void ld_global_nc_v8(const void* src, uint32_t* v) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7])
+               : "l"(src));
+}
 
 // 32-byte global store (one full sector per thread); `dst` 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8]) {
@@ -645,25 +654,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // Q of this unit: latent dims into TMEM cols 0..255, rope dims into smem
           if (nseg > 0 && !group_all(wait_bar(s, B_QFREE, (uint32_t)((nseg - 1) & 1), p))) break;
           {
-            const uint4* qrow = reinterpret_cast<const uint4*>(
-                p.q + ((long long)b * p.rows + (valid ? row : 0)) * kD);
+            // one row per thread, read in 32-byte pieces (whole sectors) when q allows it
+            const uint16_t* qrow = p.q + ((long long)b * p.rows + (valid ? row : 0)) * kD;
+            const bool v8 = p.q_v8 != 0;
             for (int c32 = 0; c32 < 8; ++c32) {
               uint32_t v[32];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                uint4 x = valid ? __ldg(qrow + c32 * 8 + k) : make_uint4(0, 0, 0, 0);
-                v[4 * k] = x.x;
-                v[4 * k + 1] = x.y;
-                v[4 * k + 2] = x.z;
-                v[4 * k + 3] = x.w;
+              for (int k = 0; k < 4; ++k) {
+                const uint16_t* src = qrow + c32 * 64 + k * 16;
+                if (!valid) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[8 * k + e] = 0u;
+                } else if (v8) {
+                  ld_global_nc_v8(src, v + 8 * k);
+                } else {
+                  const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(src));
+                  const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+                  v[8 * k] = x0.x; v[8 * k + 1] = x0.y; v[8 * k + 2] = x0.z; v[8 * k + 3] = x0.w;
+                  v[8 * k + 4] = x1.x; v[8 * k + 5] = x1.y; v[8 * k + 6] = x1.z; v[8 * k + 7] = x1.w;
+                }
               }
               tmem_st32(tmem + lane_off + c32 * 32, v);
             }
             uint8_t* rope = s.ptr + kOffQRope + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint4 x = valid ? __ldg(qrow + 64 + j) : make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(rope + ((j ^ (r & 7)) << 4)) = x;
+            for (int j = 0; j < 4; ++j) {
+              uint32_t x[8];
+              const uint16_t* src = qrow + kDv + j * 16;
+              if (!valid) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = 0u;
+              } else if (v8) {
+                ld_global_nc_v8(src, x);
+              } else {
+                const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(src));
+                const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+              }
+              *reinterpret_cast<uint4*>(rope + (((2 * j) ^ (r & 7)) << 4)) = make_uint4(x[0], x[1], x[2], x[3]);
+              *reinterpret_cast<uint4*>(rope + (((2 * j + 1) ^ (r & 7)) << 4)) = make_uint4(x[4], x[5], x[6], x[7]);
             }
             tmem_wait_st();
             fence_proxy_async_smem();
@@ -985,7 +1015,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + lane_off + c32 * 32, v);
             tmem_wait_ld();
             if (!valid) continue;
-            // one row per thread: 32-byte stores write whole sectors
+            // one row per thread: 32-byte stores write whole sectors (out only when it is
+            // 32-byte aligned; the workspace always is)
             if (it.single) {
               uint16_t* dst = p.out + ((long long)b * p.rows + row) * kDv + c32 * 32;
 #pragma unroll
@@ -995,7 +1026,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 8; ++e)
                   w[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]) * inv,
                                      __uint_as_float(v[16 * q + 2 * e + 1]) * inv);
-                st_global_v8(dst + 16 * q, w);
+                if (p.out_v8) {
+                  st_global_v8(dst + 16 * q, w);
+                } else {
+                  reinterpret_cast<uint4*>(dst + 16 * q)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                  reinterpret_cast<uint4*>(dst + 16 * q)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
               }
             } else {
               float* dst = p.ws_o + ((long long)it.slot * kM + r) * kDv + c32 * 32;
@@ -1161,6 +1197,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.row_tiles = (p.rows + kM - 1) / kM;
   p.units = a.B * p.row_tiles;
   p.box_rows = a.block_size < 64 ? a.block_size : 64;
+  p.q_v8 = (reinterpret_cast<uintptr_t>(a.q) % 32 == 0) ? 1 : 0;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.lse_mul = a.lse_base_e ? 0.6931471805599453f : 1.0f;
   p.out = a.out;

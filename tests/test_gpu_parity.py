@@ -213,6 +213,33 @@ def test_decode_edge_cases(q_len, lengths, cp, H_, bs, kernel):
     _check_workload(w)
 
 
+def _offset_16(t):
+    """A copy of t whose data starts 16 bytes past a 32-byte boundary."""
+    big = torch.empty(t.numel() + 32, dtype=t.dtype, device=t.device)
+    base = (32 - big.data_ptr() % 32) % 32 // t.element_size()
+    view = big[base + 16 // t.element_size():][:t.numel()].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+@pytest.mark.parametrize("with_workspace", [True, False])
+def test_decode_q_and_out_only_16_byte_aligned(with_workspace, kernel):
+    # q and out need only 16-byte alignment; wider accesses must not be assumed
+    w = synth.make_workload("plain", lengths=[1000, 2049])
+    step = _gpu_shards(w, with_workspace)
+    q16 = _offset_16(step.q)
+    out16 = _offset_16(torch.zeros(step.partials[0].shape, dtype=torch.bfloat16, device=DEV))
+    lse = torch.empty(step.lses[0].shape, dtype=torch.float32, device=DEV)
+    M.mla_decode(q16, step.pools[0], step.block_table, step.seq_lens[0], step.gseq, step.q_len,
+                 step.cp, 0, step.scale, out=out16, lse=lse, lse_base_e=step.lse_base_e,
+                 workspace=step.workspace)
+    torch.cuda.synchronize()
+    ro, rl, _, _ = H.oracle_shards(w)
+    H.compare(out16, lse, ro[0], rl[0], False, "16-byte aligned q / out")
+    assert M.device_status() == 0
+
+
 def test_decode_block_table_with_wide_stride(kernel):
     w = synth.make_custom(2, 64, 2, [300, 129], 64, 2, seed=5, spare_columns=9)
     _check_workload(w)
