@@ -32,7 +32,7 @@
 //
 // Both CTAs compute every key exactly once for QK (576 dims) and once for PV (512 dims).
 // Work is balanced statically: the 64-key tiles of all units are concatenated and cluster
-// c takes tiles [c*T/C, (c+1)*T/C); a unit cut between clusters leaves fp32 partials
+// c takes tiles [c*T/C, (c+1)*T/C); a unit cut between clusters leaves bf16 partials
 // (normalised out + base-2 LSE) in the workspace that the combine kernel merges.
 //
 // Safety: every wait is bounded (sm100.cuh); an abort word in each CTA (set on timeout,
@@ -133,7 +133,7 @@ struct Params {
   long long* hdr;      // workspace header: [0] = total tiles T of this call
   int2* meta;          // [units] first / last cluster of each unit
   float* ws_lse;       // [units + C][128]
-  float* ws_o;         // [units + C][128][512]
+  uint16_t* ws_o;      // [units + C][128][512] normalised partial outputs, bf16
   unsigned int* status;
 };
 
@@ -1005,7 +1005,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar_addr(s.base, B_CORRDONE));
           }
           if (!ok) break;
-          // epilogue: O * (1/l) -> out (single segment) or fp32 partial
+          // epilogue: O * (1/l) -> out (single segment) or a bf16 partial
           ok = warp_all(wait_bar(s, B_OFINAL, (uint32_t)(nseg & 1), p));
           if (!ok) break;
           tc_fence_after();
@@ -1034,13 +1034,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
               }
             } else {
-              float* dst = p.ws_o + ((long long)it.slot * kM + r) * kDv + c32 * 32;
+              uint16_t* dst = p.ws_o + ((long long)it.slot * kM + r) * kDv + c32 * 32;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int q = 0; q < 2; ++q) {
                 uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[8 * q + e]) * inv);
-                st_global_v8(dst + 8 * q, w);
+                for (int e = 0; e < 8; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(v[16 * q + 2 * e]) * inv,
+                                     __uint_as_float(v[16 * q + 2 * e + 1]) * inv);
+                st_global_v8(dst + 16 * q, w);
               }
             }
           }
@@ -1108,19 +1110,19 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
       const float w = exp2f(p.ws_lse[(long long)(u + cc) * kM + r] - mx);
       if (w == 0.f) continue;
       wsum += w;
-      const float* src = p.ws_o + ((long long)(u + cc) * kM + r) * kDv;
+      const uint16_t* src = p.ws_o + ((long long)(u + cc) * kM + r) * kDv;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(src + 256 * h + 8 * lane));
-        const float4 c4 = __ldcs(reinterpret_cast<const float4*>(src + 256 * h + 8 * lane + 4));
-        acc[8 * h + 0] = fmaf(w, a.x, acc[8 * h + 0]);
-        acc[8 * h + 1] = fmaf(w, a.y, acc[8 * h + 1]);
-        acc[8 * h + 2] = fmaf(w, a.z, acc[8 * h + 2]);
-        acc[8 * h + 3] = fmaf(w, a.w, acc[8 * h + 3]);
-        acc[8 * h + 4] = fmaf(w, c4.x, acc[8 * h + 4]);
-        acc[8 * h + 5] = fmaf(w, c4.y, acc[8 * h + 5]);
-        acc[8 * h + 6] = fmaf(w, c4.z, acc[8 * h + 6]);
-        acc[8 * h + 7] = fmaf(w, c4.w, acc[8 * h + 7]);
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(src + 256 * h + 8 * lane));
+        // bf16 -> fp32 is the upper half of the word
+        acc[8 * h + 0] = fmaf(w, __uint_as_float(a.x << 16), acc[8 * h + 0]);
+        acc[8 * h + 1] = fmaf(w, __uint_as_float(a.x & 0xffff0000u), acc[8 * h + 1]);
+        acc[8 * h + 2] = fmaf(w, __uint_as_float(a.y << 16), acc[8 * h + 2]);
+        acc[8 * h + 3] = fmaf(w, __uint_as_float(a.y & 0xffff0000u), acc[8 * h + 3]);
+        acc[8 * h + 4] = fmaf(w, __uint_as_float(a.z << 16), acc[8 * h + 4]);
+        acc[8 * h + 5] = fmaf(w, __uint_as_float(a.z & 0xffff0000u), acc[8 * h + 5]);
+        acc[8 * h + 6] = fmaf(w, __uint_as_float(a.w << 16), acc[8 * h + 6]);
+        acc[8 * h + 7] = fmaf(w, __uint_as_float(a.w & 0xffff0000u), acc[8 * h + 7]);
       }
     }
   }
@@ -1157,7 +1159,7 @@ size_t tc_ws_bytes(int units, int clusters) {
   size_t b = 256;                                        // header
   b += ((size_t)units * sizeof(int2) + 255) / 256 * 256;
   b += (slots * kM * sizeof(float) + 255) / 256 * 256;
-  b += slots * kM * kDv * sizeof(float);
+  b += slots * kM * kDv * sizeof(uint16_t);
   return b;
 }
 
@@ -1244,7 +1246,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     ws += ((size_t)p.units * sizeof(int2) + 255) / 256 * 256;
     p.ws_lse = reinterpret_cast<float*>(ws);
     ws += (slots * kM * sizeof(float) + 255) / 256 * 256;
-    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_o = reinterpret_cast<uint16_t*>(ws);
     p.whole_units = 0;
   } else {
     p.hdr = nullptr;
