@@ -12,11 +12,12 @@
 // fp32 accumulator O of 128 rows x 512 dims fills one SM's whole tensor memory, leaving
 // no room for S.  So each unit runs on a CTA pair (a cluster of two SMs):
 //
-//   CTA 0 (the S-CTA) keeps Q's 512 latent dims in TMEM as the A operand (256 columns),
-//     Q's 64 rope dims in shared memory, and two 64-column S buffers.  A TMA warp streams
-//     the keys (9 chunks of 64 keys x 64 dims per tile, 128-byte swizzle, one 3-D box per
-//     3 chunks) through a ring of 7 three-chunk slots, each freed as soon as its MMAs
-//     complete; the MMA warp issues 36 MMAs (M=128, N=64, K=16) per tile into S; four
+//   CTA 0 (the S-CTA) keeps Q in TMEM as the A operand (512 latent dims in 256 columns,
+//     64 rope dims in 32) and two 64-column S buffers.  A TMA warp streams, for each unit,
+//     Q (9 chunks of 128 rows x 64 dims) and then the keys (9 chunks of 64 keys x 64 dims
+//     per tile, 128-byte swizzle, one 3-D box per 3 chunks) through a ring of 7 slots,
+//     each freed as soon as the tcgen05.cp that moves a Q chunk into TMEM or the MMAs of
+//     a key group complete; the MMA warp issues 36 MMAs (M=128, N=64, K=16) per tile into S; four
 //     softmax warps (one query row per thread) read S, apply the per-row causal bound,
 //     keep the running max / sum (online softmax in base 2 against a per-row reference
 //     max, set 2^64 above a tile's max and moved only when a tile's max exceeds it by more
@@ -72,13 +73,14 @@ constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages i
 constexpr float kRescaleThreshold = 32.0f;    // log2 units: P <= 2^32
 constexpr float kMaxHeadroom = 64.0f;         // reference max set this far above a tile max
 constexpr int kThreads = 256;
+constexpr uint32_t kColRope = 384;  // TMEM columns: Q latent 0..255, S 256..383, Q rope 384..415
 constexpr int kEvCorrect = 1;
 constexpr int kEvFinal = 2;
 
 // shared memory layout (identical offsets in both CTAs of a pair)
 constexpr int kOffRing = 0;                                  // 7 x 24 KB (S) / 5 x 32 KB (O)
-constexpr int kOffQRope = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032
-constexpr int kOffP = kOffQRope + kM * 128;                  // 188416
+constexpr int kOffSpare = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032: unused 16 KB
+constexpr int kOffP = kOffSpare + kM * 128;                  // 188416
 constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 225280
 constexpr int kOffPR = kVGroups * 4 * kChunkBytes;           // 163840: O-CTA receive slots
 static_assert(kOffPR + kPRecv * kPSlotBytes <= kOffBar, "O-CTA receive slots");
@@ -93,8 +95,6 @@ enum Bar : int {
   B_KEMPTY = 7,           // [7]
   B_SFULL = 14,           // [2]
   B_SFREE = 16,           // [2]
-  B_QREADY = 18,
-  B_QFREE = 19,
   B_PFREE = 20,           // [3]  (arrived by the O-CTA's multicast commit)
   // O-CTA
   B_VFULL = 23,           // [5] per half-tile value group
@@ -125,7 +125,7 @@ struct Params {
   int whole_units;     // 1: no workspace, each cluster takes whole units round-robin
   int box_rows;        // rows per TMA box = min(bs, 64)
   int kz, vz;          // chunks per K / V TMA box (3 and 4, or 1 when a page is < 64 rows)
-  int q_v8, out_v8;    // q / out are 32-byte aligned: rows are read / written in 32-byte pieces
+  int out_v8;          // out is 32-byte aligned: output rows are written in 32-byte pieces
   float scale_log2;
   float lse_mul;
   uint16_t* out;
@@ -136,14 +136,6 @@ struct Params {
   uint16_t* ws_o;      // [units + C][128][512] normalised partial outputs, bf16
   unsigned int* status;
 };
-
-// 32-byte read-only global load (one full sector per thread); `src` 32-byte aligned.
-__device__ __forceinline__ void ld_global_nc_v8(const void* src, uint32_t* v) {
-  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                 "=r"(v[7])
-               : "l"(src));
-}
 
 // 32-byte global store (one full sector per thread); `dst` 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8]) {
@@ -369,7 +361,8 @@ __device__ bool seg_next(const Params& p, SegIter& it) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap, const Params p) {
+                         const __grid_constant__ CUtensorMap vmap,
+                         const __grid_constant__ CUtensorMap qmap, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SmemCtx s;
   s.ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -407,8 +400,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_addr(s.base, B_PSTAGED + i), 4);
       mbar_init(bar_addr(s.base, B_STAGEFREE + i), 1);
     }
-    mbar_init(bar_addr(s.base, B_QREADY), 4);
-    mbar_init(bar_addr(s.base, B_QFREE), 1);
     mbar_init(bar_addr(s.base, B_PVDONE), 1);
     mbar_init(bar_addr(s.base, B_EV), 1);
     mbar_init(bar_addr(s.base, B_CORRDONE), 4);
@@ -512,6 +503,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (seg_first(p, c, it, T, s_scan)) {
         do {
           win.start(p, it);
+          // the unit's Q (128 rows x 576 dims) first: 9 chunks of 64 dims, one per ring
+          // slot, which the MMA warp copies into TMEM
+          const int qy = (it.u / p.row_tiles) * p.rows + (it.u % p.row_tiles) * kM;
+          for (int qc = 0; qc < kKChunks && okk; ++qc) {
+            okk = warp_all(wait_bar(s, B_KEMPTY + slot, par, p));
+            if (!okk) break;
+            const uint32_t fb = bar_addr(s.base, B_KFULL + slot);
+            mbar_arrive_expect_tx_warp(fb, kM * 128);
+            tma_load_2d_warp(s.base + kOffRing + slot * kKGroup * kChunkBytes, &qmap, qc * 64, qy, fb);
+            ++issued;
+            if (++slot == kKGroups) {
+              slot = 0;
+              par ^= 1u;
+            }
+          }
           for (int t = it.t_begin; t < it.t_end && okk; ++t) {
             int ys[4];
             win.tile_rows(p, t, ys);
@@ -548,14 +554,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       long long n = 0;
       int nseg = 0;
       const uint32_t idesc = idesc_bf16(kM, kTile, false, false);
-      const uint32_t qrope = s.base + kOffQRope;
       int kslot = 0;          // key group slot of the next group, and its phase parity
       uint32_t kpar = 0;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
-          if (!warp_all(wait_bar(s, B_QREADY, (uint32_t)(nseg & 1), p))) break;
-          tc_fence_after();
+          // the unit's Q: 9 chunks from the ring into TMEM (latent dims at columns 0..255,
+          // rope dims at kColRope); in issue order after the previous unit's last QK
           bool ok = true;
+          for (int qc = 0; qc < kKChunks && ok; ++qc) {
+            ok = warp_all(wait_bar(s, B_KFULL + kslot, kpar, p));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t qb = s.base + kOffRing + kslot * kKGroup * kChunkBytes;
+            const uint32_t tq = tmem + (qc < 8 ? (uint32_t)qc * 32 : kColRope);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tmem_cp_128x256b_warp(tq + 8 * k, smem_desc(qb + 32 * k, 16, 1024, kSwizzle128B));
+            mma_commit_warp(bar_addr(s.base, B_KEMPTY + kslot));
+            if (++kslot == kKGroups) {
+              kslot = 0;
+              kpar ^= 1u;
+            }
+          }
+          if (!ok) break;
           for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
             const int g = (int)(n & 1);
             ok = warp_all(wait_bar(s, B_SFREE + g, (uint32_t)(((n >> 1) + 1) & 1), p));
@@ -574,19 +595,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int cc = 0; cc < kKGroup; ++cc) {
                 const int ch = kKGroup * gi + cc;
                 const uint64_t b0 = smem_desc(gb + cc * kChunkBytes, 16, 1024, kSwizzle128B);
-                if (ch < 8) {
-                  const uint32_t a0 = tmem + ch * 32;
-                  mma_ts_warp(d, a0, b0, idesc, ch != 0);
-                  mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
-                  mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
-                  mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
-                } else {
-                  const uint64_t a0 = smem_desc(qrope, 16, 1024, kSwizzle128B);
-                  mma_ss_warp(d, a0, b0, idesc, 1);
-                  mma_ss_warp(d, a0 + 2, b0 + 2, idesc, 1);
-                  mma_ss_warp(d, a0 + 4, b0 + 4, idesc, 1);
-                  mma_ss_warp(d, a0 + 6, b0 + 6, idesc, 1);
-                }
+                const uint32_t a0 = tmem + (ch < 8 ? (uint32_t)ch * 32 : kColRope);
+                mma_ts_warp(d, a0, b0, idesc, ch != 0);
+                mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
+                mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
+                mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
               }
               mma_commit_warp(bar_addr(s.base, B_KEMPTY + kslot));   // this group's slot is free
               if (++kslot == kKGroups) {
@@ -598,7 +611,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit_warp(bar_addr(s.base, B_SFULL + g));
           }
           if (!ok || !warp_all(*s.abort == 0)) break;
-          mma_commit_warp(bar_addr(s.base, B_QFREE));
           ++nseg;
         } while (seg_next(p, it));
       }
@@ -650,57 +662,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int Lr = valid ? row_bound(p, row, G, cap) : 0;
           const int seg_end_tok = it.t_end * kTile;
           const int lim_row = min(Lr, seg_end_tok);
-
-          // Q of this unit: latent dims into TMEM cols 0..255, rope dims into smem
-          if (nseg > 0 && !group_all(wait_bar(s, B_QFREE, (uint32_t)((nseg - 1) & 1), p))) break;
-          {
-            // one row per thread, read in 32-byte pieces (whole sectors) when q allows it
-            const uint16_t* qrow = p.q + ((long long)b * p.rows + (valid ? row : 0)) * kD;
-            const bool v8 = p.q_v8 != 0;
-            for (int c32 = 0; c32 < 8; ++c32) {
-              uint32_t v[32];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint16_t* src = qrow + c32 * 64 + k * 16;
-                if (!valid) {
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) v[8 * k + e] = 0u;
-                } else if (v8) {
-                  ld_global_nc_v8(src, v + 8 * k);
-                } else {
-                  const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(src));
-                  const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-                  v[8 * k] = x0.x; v[8 * k + 1] = x0.y; v[8 * k + 2] = x0.z; v[8 * k + 3] = x0.w;
-                  v[8 * k + 4] = x1.x; v[8 * k + 5] = x1.y; v[8 * k + 6] = x1.z; v[8 * k + 7] = x1.w;
-                }
-              }
-              tmem_st32(tmem + lane_off + c32 * 32, v);
-            }
-            uint8_t* rope = s.ptr + kOffQRope + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t x[8];
-              const uint16_t* src = qrow + kDv + j * 16;
-              if (!valid) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = 0u;
-              } else if (v8) {
-                ld_global_nc_v8(src, x);
-              } else {
-                const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(src));
-                const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-              }
-              *reinterpret_cast<uint4*>(rope + (((2 * j) ^ (r & 7)) << 4)) = make_uint4(x[0], x[1], x[2], x[3]);
-              *reinterpret_cast<uint4*>(rope + (((2 * j + 1) ^ (r & 7)) << 4)) = make_uint4(x[4], x[5], x[6], x[7]);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_addr(s.base, B_QREADY));
-          }
 
           float m_ref = kNegInf, l = 0.f;
           bool aborted = false;
@@ -1199,7 +1160,6 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.row_tiles = (p.rows + kM - 1) / kM;
   p.units = a.B * p.row_tiles;
   p.box_rows = a.block_size < 64 ? a.block_size : 64;
-  p.q_v8 = (reinterpret_cast<uintptr_t>(a.q) % 32 == 0) ? 1 : 0;
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.lse_mul = a.lse_base_e ? 0.6931471805599453f : 1.0f;
@@ -1283,7 +1243,23 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, p);
+  // Q as [B * q_len * H rows][576]: a unit's 128 rows of one 64-dim chunk per box (rows
+  // past the tensor read as zeros; rows of the next request in a partial unit are loaded
+  // but belong to rows the unit never stores)
+  CUtensorMap qmap;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * p.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kM};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = get_encoder()(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                               const_cast<uint16_t*>(a.q), dims, strides, box, es,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = (long long)p.units * kM;

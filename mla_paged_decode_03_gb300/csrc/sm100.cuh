@@ -363,6 +363,18 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Copies a 128-row x 256-bit block from shared memory (matrix descriptor `desc`, the
+// layout of an MMA operand) into TMEM lanes 0..127, 8 columns from `taddr`.  Ordered with
+// the issuing thread's MMAs (tcgen05 operations of one thread execute in issue order);
+// tcgen05.commit reports its completion.  Warp-collective, one elected lane issues.
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t desc) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}" ::"r"(taddr),
+      "l"(desc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
