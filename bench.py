@@ -244,8 +244,8 @@ def time_e2e(step, steps, warmup, flush):
 # call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
 # source they were taken on: a changed kernel reports null until it is captured again.
 TRAFFIC = {
-    # commit a338e17: decode 21,960,021 + 7,595 B, combine 23,132,501 B (mean of 3 calls)
-    ("cp2", "787006f050d6acc14cded71ef1496a5cf13aa6be04f2d71ef575f0a885a33bdf"): 45100117,
+    # commit 2c501b0: decode 21,959,851 B read, combine 11,601,152 B read (mean of 3 calls)
+    ("cp2", "5a2c01c5d66cab5967dcfc26344dd976771f9646c225415b862a029119f2d7fb"): 33561003,
 }
 
 
