@@ -122,7 +122,8 @@ struct Params {
   int row_tiles;       // ceil(rows / 128)
   int units;           // B * row_tiles
   int clusters;        // C
-  int whole_units;     // 1: no workspace, each cluster takes whole units round-robin
+  int groups;          // G = clusters / row_tiles: clusters g*R .. g*R+R-1 form group g
+  int whole_units;     // 1: no workspace, each group takes whole requests round-robin
   int box_rows;        // rows per TMA box = min(bs, 64)
   int kz, vz;          // chunks per K / V TMA box (3 and 4, or 1 when a page is < 64 rows)
   int out_v8;          // out is 32-byte aligned: output rows are written in 32-byte pieces
@@ -175,28 +176,99 @@ __device__ __forceinline__ int unit_tiles(const Params& p, int u) {
   return (unit_keys(p, u) + kTile - 1) / kTile;
 }
 
-// Iterates the segments (unit, tile range) that cluster c owns, in order.  Each role of
-// both CTAs of the pair runs its own copy of the iterator and sees the same sequence.
+// Tiles of request b: those of its last row tile, which sees the most keys (rows are
+// ordered by query position, and a later position sees one more key).
+__device__ __forceinline__ int req_tiles(const Params& p, int b) {
+  return unit_tiles(p, b * p.row_tiles + p.row_tiles - 1);
+}
+
+// Work split.  The clusters form G groups of R = row_tiles clusters; group g takes the
+// request tiles [g*T/G, (g+1)*T/G) of the concatenation of all requests' tiles, and its
+// cluster g*R + rt runs row tile rt of those tiles, so that the R units of a request read
+// the same keys at the same time (from L2 after the first).  A unit's range is clamped to
+// its own tile count (at most one fewer than its request's).  SegIter walks the segments
+// (unit, tile range) of one cluster in order; every role of both CTAs of the pair runs its
+// own copy of it and sees the same sequence.
 struct SegIter {
-  int u;            // current unit
+  int u;            // current unit = b * row_tiles + rt
+  int b;            // its request
+  int rt;           // this cluster's row tile
+  int grp;          // this cluster's group
   int t_begin;      // first tile of the segment within the unit
   int t_end;        // one past the last tile
-  long long g0;     // global index of the unit's first tile
-  long long g_end;  // end of this cluster's global tile range
-  int c;
-  int stride_units; // whole-unit mode: clusters
+  long long g0;     // index of request b's first tile in the concatenation
+  long long g_end;  // end of the group's range
   bool whole;
   bool single;      // the segment covers the whole unit
-  int slot;         // workspace slot of a partial
+  int slot;         // workspace slot of a partial: (b + grp) * R + rt
 };
 
 __device__ __forceinline__ long long range_start(long long T, int c, int C) {
   return T * c / C;
 }
 
-// Index of the cluster that owns global tile x.
+// Index of the group that owns request tile x.
 __device__ __forceinline__ int owner_of(long long x, long long T, int C) {
   return (int)(((x + 1) * C - 1) / T);
+}
+
+// Sets the segment of request it.b from tile tb, clamped to the unit's tiles; false if
+// that leaves nothing.
+__device__ __forceinline__ bool seg_set(const Params& p, SegIter& it, int tb) {
+  it.u = it.b * p.row_tiles + it.rt;
+  const int nu = unit_tiles(p, it.u);
+  int te = nu;
+  if (!it.whole) te = (int)min((long long)te, it.g_end - it.g0);
+  if (tb >= te) return false;
+  it.t_begin = tb;
+  it.t_end = te;
+  it.single = (tb == 0 && te == nu);
+  it.slot = (it.b + it.grp) * p.row_tiles + it.rt;
+  return true;
+}
+
+__device__ bool seg_next(const Params& p, SegIter& it) {
+  if (it.whole) {
+    for (int b = it.b + p.groups; b < p.B; b += p.groups) {
+      it.b = b;
+      if (seg_set(p, it, 0)) return true;
+    }
+    return false;
+  }
+  for (;;) {
+    const long long g = it.g0 + req_tiles(p, it.b);   // next request's first tile
+    if (g >= it.g_end) return false;
+    int b = it.b + 1;
+    while (b < p.B && req_tiles(p, b) == 0) ++b;
+    if (b >= p.B) return false;
+    it.b = b;
+    it.g0 = g;
+    if (seg_set(p, it, 0)) return true;
+  }
+}
+
+// First segment of cluster c, or none.  s_scan holds the request containing the group's
+// first tile and that request's first tile index (from the prologue's scan).
+__device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int* s_scan) {
+  it.grp = c / p.row_tiles;
+  it.rt = c % p.row_tiles;
+  it.whole = p.whole_units != 0;
+  if (it.grp >= p.groups) return false;
+  if (it.whole) {
+    it.g0 = 0;
+    it.g_end = 0;
+    for (int b = it.grp; b < p.B; b += p.groups) {
+      it.b = b;
+      if (seg_set(p, it, 0)) return true;
+    }
+    return false;
+  }
+  const long long a = range_start(T, it.grp, p.groups), e = range_start(T, it.grp + 1, p.groups);
+  if (a >= e || s_scan[0] < 0) return false;
+  it.b = s_scan[0];
+  it.g0 = ((long long)s_scan[2] << 32) | (unsigned)s_scan[1];
+  it.g_end = e;
+  return seg_set(p, it, (int)(a - it.g0)) || seg_next(p, it);
 }
 
 // Cache rows of a segment's TMA boxes for a producer warp: box i covers box_rows keys
@@ -291,74 +363,6 @@ __device__ __forceinline__ bool group_all(bool ok) {
   return r != 0;
 }
 
-// First segment of cluster c (scan over units), or none.
-__device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int* s_scan) {
-  it.c = c;
-  it.whole = p.whole_units != 0;
-  if (it.whole) {
-    it.stride_units = p.clusters;
-    for (int u = c; u < p.units; u += p.clusters) {
-      const int nt = unit_tiles(p, u);
-      if (nt > 0) {
-        it.u = u;
-        it.t_begin = 0;
-        it.t_end = nt;
-        it.single = true;
-        it.slot = 0;
-        return true;
-      }
-    }
-    return false;
-  }
-  const long long a = range_start(T, c, p.clusters), e = range_start(T, c + 1, p.clusters);
-  if (a >= e) return false;
-  // s_scan holds the unit containing tile a and that unit's first global tile
-  it.u = s_scan[0];
-  it.g0 = ((long long)s_scan[2] << 32) | (unsigned)s_scan[1];
-  it.g_end = e;
-  const int nt = unit_tiles(p, it.u);
-  it.t_begin = (int)(a - it.g0);
-  it.t_end = (int)min((long long)nt, e - it.g0);
-  it.single = (it.t_begin == 0 && it.t_end == nt);
-  it.slot = it.u + c;
-  return true;
-}
-
-__device__ bool seg_next(const Params& p, SegIter& it) {
-  if (it.whole) {
-    for (int u = it.u + it.stride_units; u < p.units; u += it.stride_units) {
-      const int nt = unit_tiles(p, u);
-      if (nt > 0) {
-        it.u = u;
-        it.t_begin = 0;
-        it.t_end = nt;
-        return true;
-      }
-    }
-    return false;
-  }
-  long long g = it.g0 + it.t_end;      // next global tile
-  if (g >= it.g_end) return false;
-  int u = it.u;
-  long long g0 = it.g0 + unit_tiles(p, u);
-  ++u;
-  // skip units with no tiles
-  int nt = 0;
-  while (u < p.units) {
-    nt = unit_tiles(p, u);
-    if (nt > 0) break;
-    ++u;
-  }
-  if (u >= p.units) return false;
-  it.u = u;
-  it.g0 = g0;
-  it.t_begin = 0;
-  it.t_end = (int)min((long long)nt, it.g_end - g0);
-  it.single = (it.t_end == nt);
-  it.slot = u + it.c;
-  return true;
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap,
@@ -412,7 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
 
-  // schedule: total tiles T and the unit holding this cluster's first tile
+  // schedule: total request tiles T and the request holding this group's first tile
   long long T = 0;
   {
     __shared__ long long s_total;
@@ -426,17 +430,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     // pass 1: T
     long long local = 0;
-    for (int u = tid; u < p.units; u += kThreads) local += unit_tiles(p, u);
+    for (int b = tid; b < p.B; b += kThreads) local += req_tiles(p, b);
     atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)local);
     __syncthreads();
     T = s_total;
-    if (!p.whole_units && T > 0) {
-      const long long a = range_start(T, c, p.clusters);
-      // pass 2: chunked exclusive scan to find the unit containing tile a
+    if (!p.whole_units && T > 0 && c / p.row_tiles < p.groups) {
+      const long long a = range_start(T, c / p.row_tiles, p.groups);
+      // pass 2: chunked exclusive scan to find the request containing tile a
       long long running = 0;
-      for (int base = 0; base < p.units; base += kThreads) {
-        const int u = base + tid;
-        const int nt = u < p.units ? unit_tiles(p, u) : 0;
+      for (int base = 0; base < p.B; base += kThreads) {
+        const int u = base + tid;          // a request index here
+        const int nt = u < p.B ? req_tiles(p, u) : 0;
         int incl = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -451,7 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           total += s_warp[w];
         }
         const long long excl = running + wpre + incl - nt;
-        if (u < p.units && nt > 0 && excl <= a && a < excl + nt) {
+        if (u < p.B && nt > 0 && excl <= a && a < excl + nt) {
           s_scan[0] = u;
           s_scan[1] = (int)(excl & 0xffffffffLL);
           s_scan[2] = (int)(excl >> 32);
@@ -467,8 +471,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  // meta for the combine: the owner of a unit's first tile records its cluster range;
-  // cluster 0 records T so that the combine can skip clusters with an empty tile range
+  // meta for the combine: the owner of a unit's first tile records the range of groups that
+  // hold it; cluster 0 records T so that the combine can skip groups with an empty range
   if (is_s && tid == 0 && c == 0 && !p.whole_units && p.hdr != nullptr) p.hdr[0] = T;
   if (is_s && tid == 0 && !p.whole_units && T > 0 && p.meta != nullptr) {
     SegIter it;
@@ -476,8 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       do {
         if (it.t_begin == 0) {
           const int nt = unit_tiles(p, it.u);
-          const int cf = c, cl = owner_of(it.g0 + nt - 1, T, p.clusters);
-          p.meta[it.u] = make_int2(cf, cl);
+          p.meta[it.u] = make_int2(it.grp, owner_of(it.g0 + nt - 1, T, p.groups));
         }
       } while (seg_next(p, it));
     }
@@ -1048,17 +1051,18 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
     return;
   }
   if (p.whole_units) return;
-  const int2 m = p.meta[u];
+  const int2 m = p.meta[u];                   // first and last group holding the unit
   if (m.x == m.y) return;                     // one cluster wrote the final result
-  // clusters between the first and the last owner hold a partial unless their tile
-  // range is empty (possible when there are fewer tiles than clusters)
+  // groups between the first and the last owner hold a partial unless their tile range
+  // is empty (possible when there are fewer tiles than groups); group cc's partial of
+  // unit u is in slot (b + cc) * R + rt
   const long long T = p.hdr[0];
   auto holds = [&](int cc) {
-    return range_start(T, cc, p.clusters) < range_start(T, cc + 1, p.clusters);
+    return range_start(T, cc, p.groups) < range_start(T, cc + 1, p.groups);
   };
   float mx = -INFINITY;
   for (int cc = m.x + lane; cc <= m.y; cc += 32)
-    if (holds(cc)) mx = fmaxf(mx, p.ws_lse[(long long)(u + cc) * kM + r]);
+    if (holds(cc)) mx = fmaxf(mx, p.ws_lse[((long long)(b + cc) * p.row_tiles + rt) * kM + r]);
 #pragma unroll
   for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
   float acc[16];
@@ -1068,10 +1072,10 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   if (mx != -INFINITY) {
     for (int cc = m.x; cc <= m.y; ++cc) {
       if (!holds(cc)) continue;
-      const float w = exp2f(p.ws_lse[(long long)(u + cc) * kM + r] - mx);
+      const float w = exp2f(p.ws_lse[((long long)(b + cc) * p.row_tiles + rt) * kM + r] - mx);
       if (w == 0.f) continue;
       wsum += w;
-      const uint16_t* src = p.ws_o + ((long long)(u + cc) * kM + r) * kDv;
+      const uint16_t* src = p.ws_o + (((long long)(b + cc) * p.row_tiles + rt) * kM + r) * kDv;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 a = __ldcs(reinterpret_cast<const uint4*>(src + 256 * h + 8 * lane));
@@ -1130,6 +1134,8 @@ int tc_clusters(int num_sms) { return num_sms / 2 > 0 ? num_sms / 2 : 1; }
 
 bool tc_supported(const DecodeArgs& a) {
   const int bs = a.block_size;
+  // every row tile of a request needs a cluster of its own (clusters = SMs / 2)
+  if ((a.H * a.q_len + kM - 1) / kM > a.num_sms / 2) return false;
   if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128)) return false;
   if ((long long)a.num_blocks * bs + 64 >= (1LL << 31)) return false;
   if (reinterpret_cast<uintptr_t>(a.kv) % 16 != 0) return false;
@@ -1195,6 +1201,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
       C = active;
     cudaGetLastError();
   }
+  // whole groups of row_tiles clusters (row_tiles <= C is checked by tc_supported)
+  p.groups = C / p.row_tiles;
+  C = p.groups * p.row_tiles;
   p.clusters = C;
   const size_t need = tc_ws_bytes(p.units, C);
   if (a.workspace != nullptr && a.workspace_bytes >= need) {
@@ -1214,7 +1223,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     p.ws_lse = nullptr;
     p.ws_o = nullptr;
     p.whole_units = 1;
-    if (C > p.units) C = p.units;
+    if (p.groups > p.B) p.groups = p.B;
+    C = p.groups * p.row_tiles;
     p.clusters = C;
   }
 
