@@ -240,6 +240,20 @@ def test_decode_q_and_out_only_16_byte_aligned(with_workspace, kernel):
     assert M.device_status() == 0
 
 
+@pytest.mark.parametrize("B_,H_,q_len,lengths,cp,with_ws", [
+    (1, 128, 4, [100], 1, True),        # 2 tiles, 4 row tiles: fewer tiles than groups
+    (3, 96, 4, [700, 64, 1500], 2, True),   # 3 row tiles per request: 25 groups of 3
+    (2, 48, 8, [900, 2100], 1, True),   # 3 row tiles, the last one partial
+    (4, 128, 8, [40, 333, 64, 1025], 4, True),  # 8 row tiles
+    (3, 96, 4, [700, 64, 1500], 2, False),  # whole requests per group, no workspace
+    (2, 128, 8, [300, 2000], 1, False),
+])
+def test_decode_grouped_schedule(B_, H_, q_len, lengths, cp, with_ws, kernel):
+    # clusters run in groups of ceil(q_len*H/128) (one cluster per row tile)
+    w = synth.make_custom(B_, H_, q_len, lengths, 64, cp, base_e=True, seed=B_ * 31 + H_ + q_len)
+    _check_workload(w, with_workspace=with_ws)
+
+
 def test_decode_block_table_with_wide_stride(kernel):
     w = synth.make_custom(2, 64, 2, [300, 129], 64, 2, seed=5, spare_columns=9)
     _check_workload(w)
