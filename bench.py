@@ -244,8 +244,8 @@ def time_e2e(step, steps, warmup, flush):
 # call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
 # source they were taken on: a changed kernel reports null until it is captured again.
 TRAFFIC = {
-    # commit 2c501b0: decode 21,959,851 B read, combine 11,601,152 B read (mean of 3 calls)
-    ("cp2", "5a2c01c5d66cab5967dcfc26344dd976771f9646c225415b862a029119f2d7fb"): 33561003,
+    # commit cd69e3a: decode 22,003,200 B read, combine 11,595,093 B read (mean of 3 calls)
+    ("cp2", "4ccc717658961619d7481c92e491d346ab86a58e8ab22c303bcdca78a1ee7ba8"): 33598293,
 }
 
 
