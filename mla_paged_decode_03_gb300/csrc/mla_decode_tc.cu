@@ -72,15 +72,16 @@ constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
 constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages in 2)
 constexpr float kRescaleThreshold = 32.0f;    // log2 units: P <= 2^32
 constexpr float kMaxHeadroom = 64.0f;         // reference max set this far above a tile max
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;       // warps 0-3: roles; 4-11: softmax (S-CTA) / correction (O-CTA)
 constexpr uint32_t kColRope = 384;  // TMEM columns: Q latent 0..255, S 256..383, Q rope 384..415
 constexpr int kEvCorrect = 1;
 constexpr int kEvFinal = 2;
 
 // shared memory layout (identical offsets in both CTAs of a pair)
 constexpr int kOffRing = 0;                                  // 7 x 24 KB (S) / 5 x 32 KB (O)
-constexpr int kOffSpare = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032: unused 16 KB
-constexpr int kOffP = kOffSpare + kM * 128;                  // 188416
+constexpr int kOffXchg = kOffRing + kKGroups * kKGroup * kChunkBytes;  // 172032: row max / sum
+                                                             // exchange of the softmax warps
+constexpr int kOffP = kOffXchg + kM * 128;                   // 188416
 constexpr int kOffBar = kOffP + 2 * kPSlotBytes;             // 225280
 constexpr int kOffPR = kVGroups * 4 * kChunkBytes;           // 163840: O-CTA receive slots
 static_assert(kOffPR + kPRecv * kPSlotBytes <= kOffBar, "O-CTA receive slots");
@@ -350,12 +351,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // A wait's outcome made uniform across the warp (every lane waited itself).
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
-// The same across the 128 threads of warps 4..7 (named barrier 2), so that no thread of
+// The same across the 256 threads of warps 4..11 (named barrier 2), so that no thread of
 // the group leaves a loop that the others stay in (they meet again at named barriers).
 __device__ __forceinline__ bool group_all(bool ok) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.and.pred q, 2, 128, p;\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.and.pred q, 2, 256, p;\n"
       " selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
       : "r"((uint32_t)ok)
@@ -394,21 +395,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(s.base, B_SFULL + i), 1);
-      mbar_init(bar_addr(s.base, B_SFREE + i), 4);
+      mbar_init(bar_addr(s.base, B_SFREE + i), 8);
     }
     for (int i = 0; i < kPRecv; ++i) {
       mbar_init(bar_addr(s.base, B_PFREE + i), 1);
       mbar_init(bar_addr(s.base, B_PFULL + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_addr(s.base, B_PSTAGED + i), 4);
+      mbar_init(bar_addr(s.base, B_PSTAGED + i), 8);
       mbar_init(bar_addr(s.base, B_STAGEFREE + i), 1);
     }
     mbar_init(bar_addr(s.base, B_PVDONE), 1);
     mbar_init(bar_addr(s.base, B_EV), 1);
-    mbar_init(bar_addr(s.base, B_CORRDONE), 4);
+    mbar_init(bar_addr(s.base, B_CORRDONE), 8);
     mbar_init(bar_addr(s.base, B_OFINAL), 1);
-    mbar_init(bar_addr(s.base, B_OFREE), 4);
+    mbar_init(bar_addr(s.base, B_OFREE), 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -649,9 +650,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp >= 4) {
-      // ---- softmax warps: thread = query row -----------------------------------------
-      const int r = tid - 128;                      // row within the unit, = TMEM lane
-      const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+      // ---- softmax warps: two threads per query row (warps w and w+4 share a TMEM lane
+      // quadrant), each owning 32 of a tile's 64 keys; the halves swap their row maxima
+      // (and, on a unit's last tile, their sums) through shared memory, so that both take
+      // the same decisions on the running max ---------------------------------------------
+      const int q4 = warp & 3;
+      const int hk = (warp - 4) >> 2;               // keys [32 hk, 32 hk + 32) of a tile
+      const int r = q4 * 32 + lane;                 // row within the unit, = TMEM lane
+      const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+      float* xmax = reinterpret_cast<float*>(s.ptr + kOffXchg);          // [2 tiles][2][128]
+      float* xsum = xmax + 2 * 2 * kM;                                   // [2][128]
       SegIter it;
       long long n = 0;
       int nseg = 0;
@@ -666,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int seg_end_tok = it.t_end * kTile;
           const int lim_row = min(Lr, seg_end_tok);
 
-          float m_ref = kNegInf, l = 0.f;
+          float m_ref = kNegInf, l = 0.f;           // l: this half's share of the row sum
           bool aborted = false;
           for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
             const int g = (int)(n & 1);
@@ -676,36 +684,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            uint32_t sv[64];
-            {
-              uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv);
-              uint32_t (&b2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
-              tmem_ld32(tmem + lane_off + 256 + g * kTile, a);
-              tmem_ld32(tmem + lane_off + 256 + g * kTile + 32, b2);
-            }
+            uint32_t sv[32];
+            tmem_ld32(tmem + lane_off + 256 + g * kTile + 32 * hk, sv);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(s.base, B_SFREE + g));
 
             const int t0 = t * kTile;
-            const int lim = lim_row - t0;          // valid keys of this row in the tile
+            const int lim = lim_row - t0 - 32 * hk;   // valid keys of this row in the half
             // running max on the raw scores (scale > 0 keeps the order), in log2 units;
-            // 8 independent max / sum chains keep one warp per SMSP from stalling on
-            // dependent adds
+            // 8 independent max / sum chains keep the warp from stalling on dependent ops
             float mx8[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) mx8[q] = kNegInf;
-            if (lim >= kTile) {
+            if (lim >= 32) {
 #pragma unroll
-              for (int k = 0; k < kTile; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
+              for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
             } else {
 #pragma unroll
-              for (int k = 0; k < kTile; ++k)
+              for (int k = 0; k < 32; ++k)
                 if (k < lim) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
             }
-            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+            const float hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                      fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            float* xm = xmax + (n & 1) * 2 * kM;
+            xm[hk * kM + r] = hmax;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            const float smax = fmaxf(hmax, xm[(hk ^ 1) * kM + r]);
             const float tmax = smax * p.scale_log2;
             float alpha = 1.f;
             bool resc = false;
@@ -722,10 +728,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float sum8[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
-            uint32_t pk[32];
-            if (lim >= kTile) {
+            uint32_t pk[16];
+            if (lim >= 32) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
+              for (int k = 0; k < 16; ++k) {
                 const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu));
                 const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu));
                 sum8[k & 7] += e0 + e1;
@@ -733,7 +739,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             } else {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
+              for (int k = 0; k < 16; ++k) {
                 const float e0 = 2 * k < lim
                     ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu)) : 0.f;
                 const float e1 = 2 * k + 1 < lim
@@ -742,10 +748,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pk[k] = pack_bf16x2(e0, e1);
               }
             }
-            const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-            l += sum;
+            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             const bool last = (t + 1 == it.t_end);
+            float l_row = 0.f;                     // the whole row's sum, on the last tile
+            if (last) {
+              xsum[hk * kM + r] = l;
+              asm volatile("bar.sync 1, 256;" ::: "memory");
+              l_row = l + xsum[(hk ^ 1) * kM + r];
+            }
             const bool any_resc = __any_sync(0xffffffffu, resc);
 
             // staging slot j must no longer be read by the copy of tile n-2
@@ -756,19 +767,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
             uint8_t* prow = slot + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(prow + (((4 * hk + q) ^ (r & 7)) << 4)) =
                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            float* side = reinterpret_cast<float*>(slot + kPBytes);
-            side[r] = alpha;
-            side[128 + r] = (last && l > 0.f) ? 1.f / l : 0.f;
-            int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
-            if (lane == 0) flags[warp - 4] = any_resc ? 1 : 0;
+            if (hk == 0) {
+              float* side = reinterpret_cast<float*>(slot + kPBytes);
+              side[r] = alpha;
+              side[128 + r] = (last && l_row > 0.f) ? 1.f / l_row : 0.f;
+              int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
+              if (lane == 0) flags[q4] = any_resc ? 1 : 0;
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(s.base, B_PSTAGED + j));
-            if (last && valid) {
-              const float lse2 = l > 0.f ? m_ref + log2f(l) : kNegInf;
+            if (last && valid && hk == 0) {
+              const float lse2 = l_row > 0.f ? m_ref + log2f(l_row) : kNegInf;
               const long long grow = (long long)b * p.rows + row;
               if (it.single) {
                 if (p.lse != nullptr) p.lse[grow] = lse2 * p.lse_mul;
@@ -929,9 +942,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++pv_phase;
       }
     } else if (warp >= 4) {
-      // ---- correction / epilogue warps: thread = row ---------------------------------
-      const int r = tid - 128;
-      const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+      // ---- correction / epilogue warps: thread = row; warps w and w+4 share a TMEM lane
+      // quadrant and take O's columns [256 hc, 256 hc + 256) ------------------------------
+      const int q4 = warp & 3;
+      const int hc = (warp - 4) >> 2;
+      const int r = q4 * 32 + lane;
+      const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
       const float* fin = reinterpret_cast<const float*>(s.ptr + kOffFinInvL);
       volatile int* ev_word = reinterpret_cast<volatile int*>(misc + 8);
       SegIter it;
@@ -954,7 +970,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float a = reinterpret_cast<const float*>(slot + kPBytes)[r];
             if (__any_sync(0xffffffffu, a != 1.f)) {
-              for (int c32 = 0; c32 < 16; ++c32) {
+              for (int c32 = 8 * hc; c32 < 8 * hc + 8; ++c32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_off + c32 * 32, v);
                 tmem_wait_ld();
@@ -974,7 +990,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const float inv = fin[r];
-          for (int c32 = 0; c32 < 16; ++c32) {
+          for (int c32 = 8 * hc; c32 < 8 * hc + 8; ++c32) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_off + c32 * 32, v);
             tmem_wait_ld();
