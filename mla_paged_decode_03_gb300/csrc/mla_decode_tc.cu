@@ -17,8 +17,9 @@
 //     Q (9 chunks of 128 rows x 64 dims) and then the keys (9 chunks of 64 keys x 64 dims
 //     per tile, 128-byte swizzle, one 3-D box per 3 chunks) through a ring of 7 slots,
 //     each freed as soon as the tcgen05.cp that moves a Q chunk into TMEM or the MMAs of
-//     a key group complete; the MMA warp issues 36 MMAs (M=128, N=64, K=16) per tile into S; four
-//     softmax warps (one query row per thread) read S, apply the per-row causal bound,
+//     a key group complete; the MMA warp issues 36 MMAs (M=128, N=64, K=16) per tile into
+//     S; eight softmax warps (two threads per query row, 32 keys each, swapping their row
+//     maxima through shared memory) read S, apply the per-row causal bound,
 //     keep the running max / sum (online softmax in base 2 against a per-row reference
 //     max, set 2^64 above a tile's max and moved only when a tile's max exceeds it by more
 //     than 2^32, so that P <= 2^32 and rescales of O are rare even when a few keys score
@@ -26,7 +27,7 @@
 //     staging slot, which a copy warp bulk-copies into one of three receive slots of CTA 1.
 //   CTA 1 (the O-CTA) holds O in all 512 TMEM columns.  A TMA warp streams the same keys'
 //     first 512 dims (V) through five half-tile groups; the MMA warp issues 8 MMAs (M=128,
-//     N=256, K=16) of P V per tile; four warps rescale O in TMEM on the tiles where the
+//     N=256, K=16) of P V per tile; eight warps rescale O in TMEM on the tiles where the
 //     reference max moved, and at the end of a segment read O out, scale by 1/l and
 //     store it.
 //   Both MMA warps run their loops as whole converged warps and issue through elect.sync.
