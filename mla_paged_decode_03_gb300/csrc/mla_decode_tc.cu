@@ -73,6 +73,7 @@ constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
 constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages in 2)
 constexpr float kRescaleThreshold = 32.0f;    // log2 units: P <= 2^32
 constexpr float kMaxHeadroom = 64.0f;         // reference max set this far above a tile max
+constexpr float kMaxTileSum = 4294967296.0f;  // 2^kRescaleThreshold: bound on a half-tile sum
 constexpr int kThreads = 384;       // warps 0-3: roles; 4-11: softmax (S-CTA) / correction (O-CTA)
 constexpr uint32_t kColRope = 384;  // TMEM columns: Q latent 0..255, S 256..383, Q rope 384..415
 constexpr int kEvCorrect = 1;
@@ -344,6 +345,46 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Three-input maximum (a single instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 lanes in one 64-bit register, and the paired fused multiply-add / add on them
+// (each lane rounded exactly as the scalar fmaf / +).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Named barrier 1 over the 256 softmax threads that also ORs a flag across them.
+__device__ __forceinline__ bool bar_or_256(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -401,6 +442,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPRecv; ++i) {
       mbar_init(bar_addr(s.base, B_PFREE + i), 1);
       mbar_init(bar_addr(s.base, B_PFULL + i), 1);
+      // the O-CTA expects each receive slot's first P tile (and re-arms it after each use)
+      if (crank == 1) mbar_arrive_expect_tx(bar_addr(s.base, B_PFULL + i), kPBytes + kSideBytes);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr(s.base, B_PSTAGED + i), 8);
@@ -596,15 +639,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = warp_all(wait_bar(s, B_KFULL + kslot, kpar, p));
               if (!ok) break;
               const uint32_t gb = s.base + kOffRing + kslot * kKGroup * kChunkBytes;
-#pragma unroll
-              for (int cc = 0; cc < kKGroup; ++cc) {
-                const int ch = kKGroup * gi + cc;
-                const uint64_t b0 = smem_desc(gb + cc * kChunkBytes, 16, 1024, kSwizzle128B);
-                const uint32_t a0 = tmem + (ch < 8 ? (uint32_t)ch * 32 : kColRope);
-                mma_ts_warp(d, a0, b0, idesc, ch != 0);
-                mma_ts_warp(d, a0 + 8, b0 + 2, idesc, 1);
-                mma_ts_warp(d, a0 + 16, b0 + 4, idesc, 1);
-                mma_ts_warp(d, a0 + 24, b0 + 6, idesc, 1);
+              {
+                const int ch = kKGroup * gi;
+                mma12_ts_warp(d, tmem + (uint32_t)ch * 32, tmem + (uint32_t)(ch + 1) * 32,
+                              tmem + (ch + 2 < 8 ? (uint32_t)(ch + 2) * 32 : kColRope),
+                              smem_desc(gb, 16, 1024, kSwizzle128B), idesc, gi != 0);
               }
               mma_commit_warp(bar_addr(s.base, B_KEMPTY + kslot));   // this group's slot is free
               if (++kslot == kKGroups) {
@@ -634,8 +673,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = wait_bar(s, B_PSTAGED + j, (uint32_t)((n >> 1) & 1), p) &&
                  wait_bar(s, B_PFREE + jr, (uint32_t)(((n / kPRecv) & 1) ^ 1), p, true);
             if (!ok) break;
+            // the O-CTA has armed its receive barrier for these bytes
             const uint32_t rbar = mapa(bar_addr(s.base, B_PFULL + jr), peer);
-            mbar_arrive_expect_tx_cluster(rbar, kPBytes + kSideBytes);
             bulk_s2cluster(mapa(s.base + kOffPR + jr * kPSlotBytes, peer),
                            s.base + kOffP + j * kPSlotBytes, kPBytes + kSideBytes, rbar);
             bulk_commit();
@@ -694,63 +733,110 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
             const int t0 = t * kTile;
             const int lim = lim_row - t0 - 32 * hk;   // valid keys of this row in the half
-            // running max on the raw scores (scale > 0 keeps the order), in log2 units;
-            // 8 independent max / sum chains keep the warp from stalling on dependent ops
-            float mx8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mx8[q] = kNegInf;
-            if (lim >= 32) {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
-            } else {
-#pragma unroll
-              for (int k = 0; k < 32; ++k)
-                if (k < lim) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
-            }
-            const float hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            float* xm = xmax + (n & 1) * 2 * kM;
-            xm[hk * kM + r] = hmax;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            const float smax = fmaxf(hmax, xm[(hk ^ 1) * kM + r]);
-            const float tmax = smax * p.scale_log2;
+            // Common case first: every key of both halves is valid and the running max
+            // already bounds this tile (no 2^x above 2^32, checked through the sum).  All 256
+            // threads then keep the running max, and one barrier with an OR-reduction tells
+            // them whether any row needs the full step below (a new max, a partial half, or
+            // a unit's first tile), which all of them then take.
             float alpha = 1.f;
             bool resc = false;
-            if (tmax > m_ref + kRescaleThreshold) {
-              const float m_new = tmax + kMaxHeadroom;
-              if (m_ref != kNegInf) {
-                alpha = fast_exp2(m_ref - m_new);
-                resc = true;
-              }
-              l *= alpha;
-              m_ref = m_new;
-            }
-            const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
-            float sum8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
             uint32_t pk[16];
-            if (lim >= 32) {
+            float fsum = 0.f;
+            bool fast = (lim >= 32) && (m_ref != kNegInf);
+            if (fast) {
+              const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+              const uint64_t nm2 = f32x2(-m_ref, -m_ref);
+              uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
               for (int k = 0; k < 16; ++k) {
-                const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu));
-                const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu));
-                sum8[k & 7] += e0 + e1;
+                float y0, y1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
+                                      sc2, nm2), y0, y1);
+                const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+                s2[k & 3] = add_f32x2(s2[k & 3], f32x2(e0, e1));
                 pk[k] = pack_bf16x2(e0, e1);
               }
+              float t0, t1;
+              f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), t0, t1);
+              fsum = t0 + t1;
+              fast = fsum <= kMaxTileSum;
+            }
+            const bool slow = bar_or_256(!fast);
+            if (!slow) {
+              l += fsum;
             } else {
+              // running max on the raw scores (scale > 0 keeps the order), in log2 units.  A
+              // whole half (the common case) takes three-input maxima and paired fp32
+              // arithmetic, so that these warps leave issue slots to the MMA warp that shares
+              // their scheduler; a partial half masks key by key.
+              float hmax;
+              if (lim >= 32) {
+                float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const float e0 = 2 * k < lim
-                    ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu)) : 0.f;
-                const float e1 = 2 * k + 1 < lim
-                    ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu)) : 0.f;
-                sum8[k & 7] += e0 + e1;
-                pk[k] = pack_bf16x2(e0, e1);
+                for (int k = 0; k < 32; k += 8)
+#pragma unroll
+                  for (int q = 0; q < 4; ++q)
+                    m4[q] = fmax3(m4[q], __uint_as_float(sv[k + 2 * q]), __uint_as_float(sv[k + 2 * q + 1]));
+                hmax = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+              } else {
+                float mx8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx8[q] = kNegInf;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                  if (k < lim) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
+                hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+              }
+              float* xm = xmax + (n & 1) * 2 * kM;
+              xm[hk * kM + r] = hmax;
+              asm volatile("bar.sync 1, 256;" ::: "memory");
+              const float smax = fmaxf(hmax, xm[(hk ^ 1) * kM + r]);
+              const float tmax = smax * p.scale_log2;
+              if (tmax > m_ref + kRescaleThreshold) {
+                const float m_new = tmax + kMaxHeadroom;
+                if (m_ref != kNegInf) {
+                  alpha = fast_exp2(m_ref - m_new);
+                  resc = true;
+                }
+                l *= alpha;
+                m_ref = m_new;
+              }
+              const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
+              if (lim >= 32) {
+                // e = 2^(s * scale_log2 - m) two keys per instruction (each lane rounds as fmaf)
+                const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+                const uint64_t nm2 = f32x2(neg_mu, neg_mu);
+                uint64_t s2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  float y0, y1;
+                  f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
+                                        sc2, nm2), y0, y1);
+                  const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+                  s2[k & 3] = add_f32x2(s2[k & 3], f32x2(e0, e1));
+                  pk[k] = pack_bf16x2(e0, e1);
+                }
+                float t0, t1;
+                f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), t0, t1);
+                l += t0 + t1;
+              } else {
+                float sum8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const float e0 = 2 * k < lim
+                      ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu)) : 0.f;
+                  const float e1 = 2 * k + 1 < lim
+                      ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu)) : 0.f;
+                  sum8[k & 7] += e0 + e1;
+                  pk[k] = pack_bf16x2(e0, e1);
+                }
+                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                     ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
               }
             }
-            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             const bool last = (t + 1 == it.t_end);
             float l_row = 0.f;                     // the whole row's sum, on the last tile
             if (last) {
@@ -773,8 +859,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             if (hk == 0) {
               float* side = reinterpret_cast<float*>(slot + kPBytes);
-              side[r] = alpha;
-              side[128 + r] = (last && l_row > 0.f) ? 1.f / l_row : 0.f;
+              // the O-CTA reads the factors only after a step that may rescale (taken by all
+              // rows together), and 1 / l only on a unit's last tile
+              if (slow) side[r] = alpha;
+              if (last) side[128 + r] = l_row > 0.f ? 1.f / l_row : 0.f;
               int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
               if (lane == 0) flags[q4] = any_resc ? 1 : 0;
             }
@@ -863,6 +951,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int j = (int)(n % kPRecv);       // receive slot of this tile's P
             ok = warp_all(wait_bar(s, B_PFULL + j, (uint32_t)((n / kPRecv) & 1), p, true));
             if (!ok) break;
+            // arm the slot for its next tile (the copy is issued only after this tile's PV)
+            if (lane == 0) mbar_arrive_expect_tx(bar_addr(s.base, B_PFULL + j), kPBytes + kSideBytes);
             const uint8_t* slot = s.ptr + kOffPR + j * kPSlotBytes;
             const int* flags = reinterpret_cast<const int*>(slot + kPBytes + 1024);
             const bool first = (t == it.t_begin);

@@ -363,6 +363,50 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Four TS MMAs that walk K by 16 (A: TMEM columns +8 each; B: descriptor start +32 bytes
+// each) under one election, so that the issuing warp spends fewer instructions per MMA;
+// `accumulate` applies to the first, the other three always accumulate.
+__device__ __forceinline__ void mma4_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, t, e;\n .reg .b32 a1, a2, a3;\n .reg .b64 b1, b2, b3;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.ne.b32 t, %5, 0;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+      " add.u64 b1, %2, 2;\n add.u64 b2, %2, 4;\n add.u64 b3, %2, 6;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(1u)
+      : "memory");
+}
+
+// Twelve TS MMAs of one three-chunk key group under one election: chunk c (A at TMEM
+// column a_c, B descriptor b0 advanced by c x 8 KB) times four K-steps of 16 (A columns
+// +8, B start +32 bytes).  `accumulate` applies to the first MMA only.
+__device__ __forceinline__ void mma12_ts_warp(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint64_t b0, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, t, e;\n .reg .b32 lo, hi, x, a;\n .reg .b64 b;\n"
+      " setp.ne.b32 p, %6, 0;\n setp.ne.b32 t, %7, 0;\n mov.b64 {lo, hi}, %4;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %4, %5, p;\n"
+      " add.u32 a, %1, 8; add.u32 x, lo, 2; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %1, 16; add.u32 x, lo, 4; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %1, 24; add.u32 x, lo, 6; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 x, lo, 512; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], b, %5, t;\n"
+      " add.u32 a, %2, 8; add.u32 x, lo, 514; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %2, 16; add.u32 x, lo, 516; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %2, 24; add.u32 x, lo, 518; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 x, lo, 1024; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], b, %5, t;\n"
+      " add.u32 a, %3, 8; add.u32 x, lo, 1026; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %3, 16; add.u32 x, lo, 1028; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      " add.u32 a, %3, 24; add.u32 x, lo, 1030; mov.b64 b, {x, hi};\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, t;\n"
+      "}" ::"r"(d_tmem), "r"(a0), "r"(a1), "r"(a2), "l"(b0), "r"(idesc), "r"(accumulate), "r"(1u)
+      : "memory");
+}
+
 // Copies a 128-row x 256-bit block from shared memory (matrix descriptor `desc`, the
 // layout of an MMA operand) into TMEM lanes 0..127, 8 columns from `taddr`.  Ordered with
 // the issuing thread's MMAs (tcgen05 operations of one thread execute in issue order);
