@@ -424,6 +424,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int c = (int)cluster_id_x();
   const bool is_s = (crank == 0);
 
+  // the tensor-map descriptors are fetched while the setup below runs
+  if (tid == 96) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&vmap);
+  }
+
   // ---- setup: barriers, TMEM, schedule scan -----------------------------------------
   if (tid == 0) {
     *s.abort = 0;
@@ -538,7 +545,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---- K producer: per tile 3 groups of 3 chunks, each one 3-D TMA box per page
       // part (the whole warp runs the loop; one elected lane issues) --------------------
-      if (lane == 0) prefetch_tensormap(&kmap);
       SegIter it;
       BoxWindow win;
       win.lane = lane;
@@ -550,11 +556,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nbox = kTile / p.box_rows;
       if (seg_first(p, c, it, T, s_scan)) {
         do {
-          win.start(p, it);
           // the unit's Q (128 rows x 576 dims) first: 9 chunks of 64 dims, one per ring
-          // slot, which the MMA warp copies into TMEM
+          // slot, which the MMA warp copies into TMEM; the unit's page rows are looked up
+          // while the first seven are in flight
           const int qy = (it.u / p.row_tiles) * p.rows + (it.u % p.row_tiles) * kM;
+          static_assert(kKChunks > kKGroups, "page window started inside the Q loop");
           for (int qc = 0; qc < kKChunks && okk; ++qc) {
+            if (qc == kKGroups) win.start(p, it);
             okk = warp_all(wait_bar(s, B_KEMPTY + slot, par, p));
             if (!okk) break;
             const uint32_t fb = bar_addr(s.base, B_KFULL + slot);
@@ -889,7 +897,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---- V producer: per half tile one group of 4 chunks, one 3-D TMA box per page
       // part (the whole warp runs the loop; one elected lane issues) --------------------
-      if (lane == 0) prefetch_tensormap(&vmap);
       SegIter it;
       BoxWindow win;
       win.lane = lane;
