@@ -203,6 +203,7 @@ struct SegIter {
   long long g_end;  // end of the group's range
   bool whole;
   bool single;      // the segment covers the whole unit
+  int nt;           // the unit's tile count
   int slot;         // workspace slot of a partial: (b + grp) * R + rt
 };
 
@@ -226,6 +227,7 @@ __device__ __forceinline__ bool seg_set(const Params& p, SegIter& it, int tb) {
   it.t_begin = tb;
   it.t_end = te;
   it.single = (tb == 0 && te == nu);
+  it.nt = nu;
   it.slot = (it.b + it.grp) * p.row_tiles + it.rt;
   return true;
 }
@@ -526,17 +528,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // meta for the combine: the owner of a unit's first tile records the range of groups that
   // hold it; cluster 0 records T so that the combine can skip groups with an empty range
   if (is_s && tid == 0 && c == 0 && !p.whole_units && p.hdr != nullptr) p.hdr[0] = T;
-  if (is_s && tid == 0 && !p.whole_units && T > 0 && p.meta != nullptr) {
-    SegIter it;
-    if (seg_first(p, c, it, T, s_scan)) {
-      do {
-        if (it.t_begin == 0) {
-          const int nt = unit_tiles(p, it.u);
-          p.meta[it.u] = make_int2(it.grp, owner_of(it.g0 + nt - 1, T, p.groups));
-        }
-      } while (seg_next(p, it));
-    }
-  }
 
   const float kNegInf = -INFINITY;
 
@@ -574,6 +565,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               par ^= 1u;
             }
           }
+          // for the combine: the owner of a unit's first tile records the range of groups
+          // that hold the unit (after the unit's Q is on its way)
+          if (lane == 0 && okk && it.t_begin == 0 && !it.whole && p.meta != nullptr)
+            p.meta[it.u] = make_int2(it.grp, owner_of(it.g0 + it.nt - 1, T, p.groups));
           for (int t = it.t_begin; t < it.t_end && okk; ++t) {
             int ys[4];
             win.tile_rows(p, t, ys);
@@ -1174,9 +1169,15 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   auto holds = [&](int cc) {
     return range_start(T, cc, p.groups) < range_start(T, cc + 1, p.groups);
   };
+  // lanes take one holder each (32 at a time): the LSEs in one round of loads, then every
+  // holder's partial row loaded without waiting on its weight (a non-holder's slot is
+  // read but not used), accumulated in holder order
+  auto lse_at = [&](int cc) { return p.ws_lse[((long long)(b + cc) * p.row_tiles + rt) * kM + r]; };
   float mx = -INFINITY;
-  for (int cc = m.x + lane; cc <= m.y; cc += 32)
-    if (holds(cc)) mx = fmaxf(mx, p.ws_lse[((long long)(b + cc) * p.row_tiles + rt) * kM + r]);
+  for (int cb = m.x; cb <= m.y; cb += 32) {
+    const int cc = cb + lane;
+    if (cc <= m.y && holds(cc)) mx = fmaxf(mx, lse_at(cc));
+  }
 #pragma unroll
   for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
   float acc[16];
@@ -1184,24 +1185,32 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   float wsum = 0.f;
   if (mx != -INFINITY) {
-    for (int cc = m.x; cc <= m.y; ++cc) {
-      if (!holds(cc)) continue;
-      const float w = exp2f(p.ws_lse[((long long)(b + cc) * p.row_tiles + rt) * kM + r] - mx);
-      if (w == 0.f) continue;
-      wsum += w;
-      const uint16_t* src = p.ws_o + (((long long)(b + cc) * p.row_tiles + rt) * kM + r) * kDv;
+    for (int cb = m.x; cb <= m.y; cb += 32) {
+      const int cc = cb + lane;
+      const float wl = (cc <= m.y && holds(cc)) ? exp2f(lse_at(cc) - mx) : 0.f;
+      const int nh = min(32, m.y - cb + 1);
+#pragma unroll 4
+      for (int k = 0; k < nh; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        const uint16_t* src = p.ws_o + (((long long)(b + cb + k) * p.row_tiles + rt) * kM + r) * kDv;
+        const uint4 a0 = __ldcs(reinterpret_cast<const uint4*>(src + 8 * lane));
+        const uint4 a1 = __ldcs(reinterpret_cast<const uint4*>(src + 256 + 8 * lane));
+        if (w == 0.f) continue;
+        wsum += w;
+        const uint4 av[2] = {a0, a1};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(src + 256 * h + 8 * lane));
-        // bf16 -> fp32 is the upper half of the word
-        acc[8 * h + 0] = fmaf(w, __uint_as_float(a.x << 16), acc[8 * h + 0]);
-        acc[8 * h + 1] = fmaf(w, __uint_as_float(a.x & 0xffff0000u), acc[8 * h + 1]);
-        acc[8 * h + 2] = fmaf(w, __uint_as_float(a.y << 16), acc[8 * h + 2]);
-        acc[8 * h + 3] = fmaf(w, __uint_as_float(a.y & 0xffff0000u), acc[8 * h + 3]);
-        acc[8 * h + 4] = fmaf(w, __uint_as_float(a.z << 16), acc[8 * h + 4]);
-        acc[8 * h + 5] = fmaf(w, __uint_as_float(a.z & 0xffff0000u), acc[8 * h + 5]);
-        acc[8 * h + 6] = fmaf(w, __uint_as_float(a.w << 16), acc[8 * h + 6]);
-        acc[8 * h + 7] = fmaf(w, __uint_as_float(a.w & 0xffff0000u), acc[8 * h + 7]);
+        for (int h = 0; h < 2; ++h) {
+          const uint4 a = av[h];
+          // bf16 -> fp32 is the upper half of the word
+          acc[8 * h + 0] = fmaf(w, __uint_as_float(a.x << 16), acc[8 * h + 0]);
+          acc[8 * h + 1] = fmaf(w, __uint_as_float(a.x & 0xffff0000u), acc[8 * h + 1]);
+          acc[8 * h + 2] = fmaf(w, __uint_as_float(a.y << 16), acc[8 * h + 2]);
+          acc[8 * h + 3] = fmaf(w, __uint_as_float(a.y & 0xffff0000u), acc[8 * h + 3]);
+          acc[8 * h + 4] = fmaf(w, __uint_as_float(a.z << 16), acc[8 * h + 4]);
+          acc[8 * h + 5] = fmaf(w, __uint_as_float(a.z & 0xffff0000u), acc[8 * h + 5]);
+          acc[8 * h + 6] = fmaf(w, __uint_as_float(a.w << 16), acc[8 * h + 6]);
+          acc[8 * h + 7] = fmaf(w, __uint_as_float(a.w & 0xffff0000u), acc[8 * h + 7]);
+        }
       }
     }
   }
