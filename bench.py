@@ -244,8 +244,9 @@ def time_e2e(step, steps, warmup, flush):
 # call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
 # source they were taken on: a changed kernel reports null until it is captured again.
 TRAFFIC = {
-    # commit cd69e3a: decode 22,003,200 B read, combine 11,595,093 B read (mean of 3 calls)
-    ("cp2", "4ccc717658961619d7481c92e491d346ab86a58e8ab22c303bcdca78a1ee7ba8"): 33598293,
+    # decode 21,967,019 B read, combine 11,601,237 B read, no DRAM writes (mean of 3 calls;
+    # profiles/dram_traffic_cp2.md)
+    ("cp2", "04422381a28086dfe44c743695c42168d7f6ae91c2c00f72c1f81f2243567c18"): 33568256,
 }
 
 
