@@ -1,8 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark: MLA paged decode, microseconds per layer-step, on GB300.
 
-A layer-step is one pass of the whole hot path over one batch: ``mla_decode`` on every
-emulated DCP shard (partial out + LSE per shard) and ``lse_merge`` of the partials.
+A layer-step is one pass of the whole hot path over one batch: every emulated DCP
+shard's partial decode (out + LSE per shard; all shards in one ``mla_decode_shards``
+launch, as the ranks of a DCP group run at the same time) and ``lse_merge`` of the
+partials.  ``per_config[...]["decode_call_us"]`` is that launch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config cp2] [--extra-configs tiny,plain,spec,long]
@@ -171,6 +173,15 @@ def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None):
         if step.cp == 1:
             step.run()
             e[1].record(stream)
+        elif step.batched:
+            m.mla_decode_shards(step.q, step.pool_all, step.block_table_all, step.seq_lens_all,
+                                step.gseq, step.q_len, step.cp, step.scale, out=step.partials,
+                                lse=step.lses, lse_base_e=step.lse_base_e,
+                                workspace=step.workspace)
+            e[1].record(stream)
+            m.lse_merge(step.partials, step.lses, out=step.out, out_lse=step.out_lse,
+                        lse_base_e=step.lse_base_e)
+            e[2].record(stream)
         else:
             for r in range(step.cp):
                 m.mla_decode(step.q, step.pools[r], step.block_table, step.seq_lens[r],
@@ -182,16 +193,18 @@ def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None):
                         lse_base_e=step.lse_base_e)
             e[step.cp + 1].record(stream)
     torch.cuda.synchronize()
+    calls = 1 if (step.cp == 1 or step.batched) else step.cp
     for k in range(steps):
         e = ev[k]
-        last = e[1] if step.cp == 1 else e[step.cp + 1]
+        last = e[1] if step.cp == 1 else e[calls + 1]
         step_ms.append(e[0].elapsed_time(last))
-        for r in range(step.cp):
+        for r in range(calls):
             call_ms.append(e[r].elapsed_time(e[r + 1]))
     assert m.device_status() == 0
     wk = work(w)
     res = dict(step_ms=step_ms, call_ms=call_ms, work=wk, w=w, step=step,
-               launches=step.kernel_launches_per_step())
+               launches=step.kernel_launches_per_step(),
+               call_shards=step.cp if (step.cp > 1 and step.batched) else 1)
     if with_e2e:
         res["e2e"] = time_e2e(step, steps, warmup, flush)
     return res
@@ -203,9 +216,8 @@ def time_e2e(step, steps, warmup, flush):
     result (out, lse) back."""
     dev = step.q.device
     h_q = step.q.cpu().pin_memory()
-    h_bt = step.block_table.cpu().pin_memory()
-    h_sl = [s.cpu().pin_memory() for s in step.seq_lens]
-    h_g = step.gseq.cpu().pin_memory()
+    d_in = step.input_tensors()
+    h_in = [t.cpu().pin_memory() for t in d_in]
     h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h_lse = torch.empty(step.out_lse.shape, dtype=step.out_lse.dtype).pin_memory()
     d_q = torch.empty_like(step.q)
@@ -213,10 +225,8 @@ def time_e2e(step, steps, warmup, flush):
 
     def one():
         d_q.copy_(h_q, non_blocking=True)
-        step.block_table.copy_(h_bt, non_blocking=True)
-        for s, hs in zip(step.seq_lens, h_sl):
-            s.copy_(hs, non_blocking=True)
-        step.gseq.copy_(h_g, non_blocking=True)
+        for t, ht in zip(d_in, h_in):
+            t.copy_(ht, non_blocking=True)
         out, lse = step.run(q=d_q)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
@@ -234,8 +244,7 @@ def time_e2e(step, steps, warmup, flush):
         b.record(stream)
         b.synchronize()
         times.append(a.elapsed_time(b))
-    h2d = (h_q.numel() * 2 + h_bt.numel() * 4 + sum(s.numel() * 4 for s in h_sl) +
-           h_g.numel() * 4)
+    h2d = h_q.numel() * 2 + sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     return dict(ms=statistics.mean(times), h2d=h2d, d2h=d2h)
 
@@ -271,8 +280,9 @@ def summarize(res, pk):
     t_tc = wk["flops"] / (pk["bf16"] * 1e12)
     roof = max(t_hbm, t_tc)
     call = statistics.mean(res["call_ms"]) * 1e-3
-    shard_flops = statistics.mean(s["flops"] for s in wk["per_shard"])
-    shard_bytes = statistics.mean(s["bytes"] for s in wk["per_shard"])
+    # one timed call covers call_shards shards (all of them when they run in one launch)
+    shard_flops = statistics.mean(s["flops"] for s in wk["per_shard"]) * res["call_shards"]
+    shard_bytes = statistics.mean(s["bytes"] for s in wk["per_shard"]) * res["call_shards"]
     bound = "tensor" if t_tc >= t_hbm else "hbm"
     return dict(us_per_step=ms * 1e3, kv_gbs=wk["kv_bytes"] / t / 1e9,
                 tflops=wk["flops"] / t / 1e12, roofline_us=roof * 1e6,
@@ -385,7 +395,9 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": s["decode_call_gbs"], "peak": pk["hbm"],
                 "unit": "GB/s", "frac": s["decode_call_gbs"] / pk["hbm"]}
     roof.update({"traffic": measured_traffic(args.config, args.batch),
-                 "kernel": "mla_decode call (split-KV decode + split combine)",
+                 "kernel": ("mla_decode_shards call (every shard's split-KV decode + split "
+                            "combine in one launch)" if res["call_shards"] > 1 else
+                            "mla_decode call (split-KV decode + split combine)"),
                  "peak_source": pk["source"] + " (burst)"})
     cpu = (cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline
                                                   and args.batch is None) else None)
@@ -397,7 +409,10 @@ def run_ours(args):
                    "q_len": res["w"].q_len, "block_size": res["w"].bs, "shards": res["w"].cp,
                    "contexts": "U[1024,8192]" if args.config == "cp2" else "see synth",
                    "l2": "flushed (512 MB write) before every timed step",
-                   "parallelism": f"replicas{ws}" if ws > 1 else "single GPU, emulated DCP shards"},
+                   "parallelism": (f"replicas{ws}" if ws > 1 else
+                                   "single GPU, emulated DCP shards (all shards in one launch)"
+                                   if res["call_shards"] > 1 else
+                                   "single GPU, emulated DCP shards")},
         "kv_gbs": s["kv_gbs"], "tflops": s["tflops"], "roofline_frac": s["roofline_frac"],
         "roofline_us": s["roofline_us"],
         "roofline": roof,

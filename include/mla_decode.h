@@ -98,6 +98,36 @@ int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * mla_decode_shards -- every shard of one emulated context-parallel decode step in a
+ * single launch (the ranks of the pages' native DCP decode, [#54012] "关键源码片段",
+ * run side by side on one GPU instead of one per GPU).  The result is exactly that of
+ *     for r in 0 .. n_shards-1:
+ *         mla_decode(q, kv_cache, block_table + r*B*bt_stride, bt_stride, seq_lens + r*B,
+ *                    causal_seqlens_global, B, H, q_len, block_size, num_blocks,
+ *                    max_blocks, n_shards, r, scale, out + r*B*q_len*H*512,
+ *                    lse ? lse + r*B*q_len*H : NULL, lse_base_e, ...)
+ * with all shards' pages in one cache.
+ *
+ * Arguments (as mla_decode unless stated):
+ *   kv_cache     bf16 [num_blocks, block_size, 576]: the pages of every shard.
+ *   block_table  int32 [n_shards*B, bt_stride], shard-major: row r*B + b holds shard r's
+ *                page ids (into kv_cache) for request b.
+ *   seq_lens     int32 [n_shards*B], shard-major token counts.
+ *   causal_seqlens_global  int32 [B]; may be NULL only if n_shards == 1.
+ *   n_shards     >= 1; shard r is rank r of cp_world = n_shards.
+ *   out          bf16 [n_shards, B*q_len, H, 512];  lse  float [n_shards, B*q_len, H] or NULL.
+ *   workspace    sized by mla_decode_workspace_size(n_shards*B, H, q_len, num_sms).
+ * Errors: as mla_decode; also MLA_ERR_INVALID_ARGUMENT for n_shards < 1 and
+ *   MLA_ERR_UNSUPPORTED when n_shards > 1 and n_shards * B * B >= 2^32.
+ */
+int mla_decode_shards(const void* q, const void* kv_cache, const int32_t* block_table,
+                      int64_t bt_stride, const int32_t* seq_lens,
+                      const int32_t* causal_seqlens_global, int B, int H, int q_len,
+                      int block_size, int num_blocks, int max_blocks, int n_shards,
+                      float scale, void* out, float* lse, int lse_base_e, void* workspace,
+                      size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * lse_merge -- combine n_shards partial results of the same rows through their LSEs.
  *
  * Defines ([#54012] "实现拆解" step 3: shards are merged across ranks and must agree on

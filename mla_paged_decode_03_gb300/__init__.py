@@ -22,7 +22,7 @@ from ._lib import PAD_SLOT_ID, MlaError  # noqa: F401
 D_QK = 576
 D_V = 512
 
-__all__ = ["mla_decode", "lse_merge", "cp_local_slot", "workspace_size", "device_status",
+__all__ = ["mla_decode", "mla_decode_shards", "lse_merge", "cp_local_slot", "workspace_size", "device_status",
            "PAD_SLOT_ID", "MlaError", "D_QK", "D_V"]
 
 
@@ -107,6 +107,58 @@ def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tenso
                       B, H, q_len, kv_cache.shape[1], kv_cache.shape[0], block_table.shape[1],
                       cp_world, cp_rank, float(scale), out.data_ptr(), _ptr(lse),
                       1 if lse_base_e else 0, workspace.data_ptr(), ws_bytes, _stream(stream))
+    _lib.check(rc)
+    return out, lse
+
+
+def mla_decode_shards(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, causal_seqlens_global: Optional[torch.Tensor],
+                      q_len: int, n_shards: int, scale: float,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      lse_base_e: bool = True, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Every shard of an emulated context-parallel step in one launch: the result equals
+    ``mla_decode`` of shard r (rank r of cp_world = n_shards) for each r.
+
+    q [B, q_len, H, 576] bf16; kv_cache [num_blocks, block_size, 576] bf16 holding all
+    shards' pages; block_table [n_shards*B, max_blocks] int32, shard-major, page ids into
+    kv_cache; seq_lens [n_shards*B] int32 shard-major; causal_seqlens_global [B] int32.
+    Returns out [n_shards, B*q_len, H, 512] bf16 and lse [n_shards, B*q_len, H] float32.
+    """
+    if q.dim() == 3:
+        q = q.view(-1, q_len, q.shape[1], q.shape[2])
+    _need(q, "q", torch.bfloat16, 4)
+    B, ql, H, D = q.shape
+    if ql != q_len or D != D_QK:
+        raise ValueError(f"q must be [B, q_len={q_len}, H, {D_QK}], got {tuple(q.shape)}")
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    if kv_cache.shape[2] != D_QK:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or not block_table.is_cuda:
+        raise TypeError("block_table must be a 2-D int32 CUDA tensor")
+    if block_table.stride(1) != 1 or block_table.shape[0] != n_shards * B:
+        raise ValueError("block_table must be [n_shards*B, max_blocks] with contiguous rows")
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if seq_lens.shape[0] != n_shards * B:
+        raise ValueError("seq_lens must be [n_shards*B]")
+    if causal_seqlens_global is not None:
+        _need(causal_seqlens_global, "causal_seqlens_global", torch.int32, 1)
+    if out is None:
+        out = torch.empty(n_shards, B * q_len, H, D_V, dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16)
+    if lse is None:
+        lse = torch.empty(n_shards, B * q_len, H, dtype=torch.float32, device=q.device)
+    _need(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = alloc_workspace(n_shards * B, H, q_len, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    L = _lib.load()
+    rc = L.mla_decode_shards(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                             block_table.stride(0), seq_lens.data_ptr(),
+                             _ptr(causal_seqlens_global), B, H, q_len, kv_cache.shape[1],
+                             kv_cache.shape[0], block_table.shape[1], n_shards, float(scale),
+                             out.data_ptr(), lse.data_ptr(), 1 if lse_base_e else 0,
+                             workspace.data_ptr(), ws_bytes, _stream(stream))
     _lib.check(rc)
     return out, lse
 

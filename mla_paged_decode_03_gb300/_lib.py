@@ -19,7 +19,8 @@ MLA_ERR_CUDA = -3
 MLA_ERR_DEVICE = -4
 PAD_SLOT_ID = -1
 
-EXPORTED = ("mla_decode_workspace_size", "mla_decode", "mla_decode_noalloc", "lse_merge",
+EXPORTED = ("mla_decode_workspace_size", "mla_decode", "mla_decode_shards", "mla_decode_noalloc",
+            "lse_merge",
             "cp_local_slot",
             "mla_get_device_status", "mla_set_decode_kernel", "mla_last_error",
             "mla_abi_version")
@@ -59,6 +60,10 @@ def load() -> ctypes.CDLL:
         lib.mla_decode.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_int, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int, c_f, c_vp, c_vp, c_int,
                                    c_vp, c_sz, c_vp]
+        lib.mla_decode_shards.restype = c_int
+        lib.mla_decode_shards.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_int, c_int,
+                                          c_int, c_int, c_int, c_int, c_int, c_f, c_vp, c_vp,
+                                          c_int, c_vp, c_sz, c_vp]
         lib.mla_decode_noalloc.restype = c_int
         lib.mla_decode_noalloc.argtypes = [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_int, c_int,
                                            c_int, c_int, c_int, c_int, c_int, c_int, c_f, c_vp,

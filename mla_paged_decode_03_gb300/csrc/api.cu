@@ -98,46 +98,49 @@ size_t mla_decode_workspace_size(int B, int H, int q_len, int num_sms) {
   return mla::decode_workspace_size(B, H, q_len, num_sms);
 }
 
-int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
-               int64_t bt_stride, const int32_t* seq_lens,
-               const int32_t* causal_seqlens_global, int B, int H, int q_len,
-               int block_size, int num_blocks, int max_blocks, int cp_world, int cp_rank,
-               float scale, void* out, float* lse, int lse_base_e, void* workspace,
-               size_t workspace_bytes, mla_stream_t stream) {
-  if (B < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: B=%d < 0", B);
-  if (H < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: H=%d < 1", H);
+// Shared by mla_decode (n_shards == 1, the given rank) and mla_decode_shards (ranks
+// 0 .. n_shards-1 of cp_world == n_shards, shard-major tables and outputs).
+static int decode_impl(const char* fn, const void* q, const void* kv_cache,
+                       const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                       const int32_t* causal_seqlens_global, int B, int H, int q_len,
+                       int block_size, int num_blocks, int max_blocks, int cp_world,
+                       int cp_rank, int n_shards, float scale, void* out, float* lse,
+                       int lse_base_e, void* workspace, size_t workspace_bytes,
+                       mla_stream_t stream) {
+  if (B < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "%s: B=%d < 0", fn, B);
+  if (H < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "%s: H=%d < 1", fn, H);
   if (q_len < 1 || q_len > MLA_MAX_Q_LEN)
     return fail(q_len < 1 ? MLA_ERR_INVALID_ARGUMENT : MLA_ERR_UNSUPPORTED,
-                "mla_decode: q_len=%d outside [1, %d]", q_len, MLA_MAX_Q_LEN);
-  if (block_size < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: block_size < 1");
-  if (num_blocks < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: num_blocks < 1");
+                "%s: q_len=%d outside [1, %d]", fn, q_len, MLA_MAX_Q_LEN);
+  if (block_size < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "%s: block_size < 1", fn);
+  if (num_blocks < 1) return fail(MLA_ERR_INVALID_ARGUMENT, "%s: num_blocks < 1", fn);
   if (max_blocks < 1 || bt_stride < max_blocks)
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: need 1 <= max_blocks (%d) <= bt_stride (%lld)",
-                max_blocks, (long long)bt_stride);
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: need 1 <= max_blocks (%d) <= bt_stride (%lld)",
+                fn, max_blocks, (long long)bt_stride);
   if ((long long)max_blocks * block_size > (1LL << 31) - 1)
-    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: max_blocks*block_size exceeds 2^31-1");
+    return fail(MLA_ERR_UNSUPPORTED, "%s: max_blocks*block_size exceeds 2^31-1", fn);
   if ((long long)num_blocks * block_size > (1LL << 40))
-    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: cache too large");
+    return fail(MLA_ERR_UNSUPPORTED, "%s: cache too large", fn);
   if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world)
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: need 0 <= cp_rank (%d) < cp_world (%d)",
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: need 0 <= cp_rank (%d) < cp_world (%d)", fn,
                 cp_rank, cp_world);
   if (!isfinite(scale) || !(scale > 0.f))
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: scale must be finite and > 0");
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: scale must be finite and > 0", fn);
   if (B == 0) return ok();
   if (!q || !kv_cache || !block_table || !seq_lens || !out)
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: null q/kv_cache/block_table/seq_lens/out");
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: null q/kv_cache/block_table/seq_lens/out", fn);
   if (causal_seqlens_global == nullptr && cp_world != 1)
     return fail(MLA_ERR_INVALID_ARGUMENT,
-                "mla_decode: causal_seqlens_global is required when cp_world > 1");
+                "%s: causal_seqlens_global is required when cp_world > 1", fn);
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16))
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: q, kv_cache and out must be 16-byte aligned");
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: q, kv_cache and out must be 16-byte aligned", fn);
   if (!aligned(block_table, 4) || !aligned(seq_lens, 4) ||
       (causal_seqlens_global && !aligned(causal_seqlens_global, 4)) || (lse && !aligned(lse, 4)))
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: misaligned int32/float argument");
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: misaligned int32/float argument", fn);
   if (workspace && !aligned(workspace, 256))
-    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode: workspace must be 256-byte aligned");
-  if ((long long)B * q_len * H > (1LL << 31) - 1)
-    return fail(MLA_ERR_UNSUPPORTED, "mla_decode: too many query rows");
+    return fail(MLA_ERR_INVALID_ARGUMENT, "%s: workspace must be 256-byte aligned", fn);
+  if ((long long)n_shards * B * q_len * H > (1LL << 31) - 1)
+    return fail(MLA_ERR_UNSUPPORTED, "%s: too many query rows", fn);
 
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
@@ -150,7 +153,8 @@ int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
   a.bt_stride = bt_stride;
   a.seq_lens = seq_lens;
   a.gseq = causal_seqlens_global ? causal_seqlens_global : seq_lens;
-  a.B = B;
+  a.B = n_shards * B;
+  a.shard_B = B;
   a.H = H;
   a.q_len = q_len;
   a.block_size = block_size;
@@ -167,8 +171,36 @@ int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
   a.num_sms = dev->num_sms;
   a.status = dev->status;
   cudaError_t e = mla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "mla_decode launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "%s launch: %s", fn, cudaGetErrorString(e));
   return ok();
+}
+
+int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+               int64_t bt_stride, const int32_t* seq_lens,
+               const int32_t* causal_seqlens_global, int B, int H, int q_len,
+               int block_size, int num_blocks, int max_blocks, int cp_world, int cp_rank,
+               float scale, void* out, float* lse, int lse_base_e, void* workspace,
+               size_t workspace_bytes, mla_stream_t stream) {
+  return decode_impl("mla_decode", q, kv_cache, block_table, bt_stride, seq_lens,
+                     causal_seqlens_global, B, H, q_len, block_size, num_blocks, max_blocks,
+                     cp_world, cp_rank, 1, scale, out, lse, lse_base_e, workspace,
+                     workspace_bytes, stream);
+}
+
+int mla_decode_shards(const void* q, const void* kv_cache, const int32_t* block_table,
+                      int64_t bt_stride, const int32_t* seq_lens,
+                      const int32_t* causal_seqlens_global, int B, int H, int q_len,
+                      int block_size, int num_blocks, int max_blocks, int n_shards,
+                      float scale, void* out, float* lse, int lse_base_e, void* workspace,
+                      size_t workspace_bytes, mla_stream_t stream) {
+  if (n_shards < 1)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "mla_decode_shards: n_shards=%d < 1", n_shards);
+  if (n_shards > 1 && B > 0 && (unsigned long long)n_shards * B * B >= (1ull << 32))
+    return fail(MLA_ERR_UNSUPPORTED, "mla_decode_shards: n_shards * B^2 must stay below 2^32");
+  return decode_impl("mla_decode_shards", q, kv_cache, block_table, bt_stride, seq_lens,
+                     causal_seqlens_global, B, H, q_len, block_size, num_blocks, max_blocks,
+                     n_shards, 0, n_shards, scale, out, lse, lse_base_e, workspace,
+                     workspace_bytes, stream);
 }
 
 int lse_merge(const void* partials, int partials_fp32, const float* lses, int n_shards,

@@ -17,6 +17,10 @@ struct DecodeArgs {
   const int32_t* seq_lens;       // [B]
   const int32_t* gseq;           // [B] global lengths (seq_lens when cp_world == 1)
   int B, H, q_len, block_size, num_blocks, max_blocks, cp_world, cp_rank;
+  // Requests per shard.  B == shard_B for one shard; a call over several shards has
+  // B = n * shard_B, and its request b is request b % shard_B of q and gseq, in shard
+  // cp_rank + b / shard_B (block_table, seq_lens, out and lse are shard-major).
+  int shard_B;
   float scale;
   uint16_t* out;                 // bf16 [B*q_len*H, 512]
   float* lse;                    // [B*q_len*H] or null

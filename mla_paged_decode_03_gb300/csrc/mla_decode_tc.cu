@@ -121,6 +121,8 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* gseq;
   int B, H, q_len, bs, num_blocks, max_blocks, cp, rank;
+  int shard_B;         // requests per shard (request b: q / gseq row b % shard_B, rank + b / shard_B)
+  unsigned shard_mul;  // 0 for one shard, else ceil(2^32 / shard_B): b / shard_B = umulhi(b, shard_mul)
   int rows;            // H * q_len
   int row_tiles;       // ceil(rows / 128)
   int units;           // B * row_tiles
@@ -153,12 +155,17 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t smem_base, int i) {
 }
 
 // Keys visible to row r (0-based within the request's q_len*H rows).
-__device__ __forceinline__ int row_bound(const Params& p, int r, long long G, int cap) {
+__device__ __forceinline__ int row_bound(const Params& p, int r, long long G, int cap, int rank) {
   const int i = r / p.H;
   long long Gi = G - (p.q_len - 1 - i);
   if (Gi < 0) Gi = 0;
-  const long long loc = Gi / p.cp + ((Gi % p.cp) > p.rank ? 1 : 0);
+  const long long loc = Gi / p.cp + ((Gi % p.cp) > rank ? 1 : 0);
   return (int)(loc < cap ? loc : cap);
+}
+
+// Shard of request b and its row in q / gseq, without a division.
+__device__ __forceinline__ int shard_of(const Params& p, int b) {
+  return (int)__umulhi((unsigned)b, p.shard_mul);
 }
 
 __device__ __forceinline__ int seq_cap(const Params& p, int b) {
@@ -172,7 +179,8 @@ __device__ __forceinline__ int seq_cap(const Params& p, int b) {
 __device__ __forceinline__ int unit_keys(const Params& p, int u) {
   const int b = u / p.row_tiles, rt = u % p.row_tiles;
   const int last_row = min((rt + 1) * kM, p.rows) - 1;
-  return row_bound(p, last_row, __ldg(p.gseq + b), seq_cap(p, b));
+  const int sh = shard_of(p, b);
+  return row_bound(p, last_row, __ldg(p.gseq + (b - sh * p.shard_B)), seq_cap(p, b), p.rank + sh);
 }
 
 __device__ __forceinline__ int unit_tiles(const Params& p, int u) {
@@ -550,7 +558,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // the unit's Q (128 rows x 576 dims) first: 9 chunks of 64 dims, one per ring
           // slot, which the MMA warp copies into TMEM; the unit's page rows are looked up
           // while the first seven are in flight
-          const int qy = (it.u / p.row_tiles) * p.rows + (it.u % p.row_tiles) * kM;
+          const int qb = it.u / p.row_tiles;
+          const int qy = (qb - shard_of(p, qb) * p.shard_B) * p.rows + (it.u % p.row_tiles) * kM;
           static_assert(kKChunks > kKGroups, "page window started inside the Q loop");
           for (int qc = 0; qc < kKChunks && okk; ++qc) {
             if (qc == kKGroups) win.start(p, it);
@@ -711,9 +720,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int b = it.u / p.row_tiles, rt = it.u % p.row_tiles;
           const int row = rt * kM + r;
           const bool valid = row < p.rows;
-          const long long G = __ldg(p.gseq + b);
+          const int sh = shard_of(p, b);
+          const long long G = __ldg(p.gseq + (b - sh * p.shard_B));
           const int cap = seq_cap(p, b);
-          const int Lr = valid ? row_bound(p, row, G, cap) : 0;
+          const int Lr = valid ? row_bound(p, row, G, cap, p.rank + sh) : 0;
           const int seg_end_tok = it.t_end * kTile;
           const int lim_row = min(Lr, seg_end_tok);
 
@@ -1278,6 +1288,13 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.gseq = a.gseq;
   p.B = a.B;
+  p.shard_B = a.shard_B;
+  // floor(b * ceil(2^32 / d) / 2^32) = floor(b / d) while b * d < 2^32, which the entry
+  // point checks for several shards (b < n * d); one shard is shard 0 throughout
+  p.shard_mul = a.shard_B == a.B
+                    ? 0u
+                    : (unsigned)((0x100000000ull + (unsigned long long)a.shard_B - 1) /
+                                 (unsigned long long)a.shard_B);
   p.H = a.H;
   p.q_len = a.q_len;
   p.bs = a.block_size;
@@ -1381,7 +1398,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   // but belong to rows the unit never stores)
   CUtensorMap qmap;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * p.rows};
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.shard_B * p.rows};
     cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)kM};
     cuuint32_t es[2] = {1, 1};

@@ -1,11 +1,14 @@
 """One decode layer-step over emulated DCP shards on a single GPU.
 
 The KV of every request is split round-robin over ``cp`` shards; each shard has its own
-paged pool (built once, outside the step).  A step is: ``mla_decode`` on every shard
+paged pool (built once, outside the step).  A step is: every shard's partial decode
 (partial out + LSE per shard) followed by ``lse_merge`` of the partials -- the same work a
 ``cp``-rank DCP group does for one attention layer, with the cross-rank exchange replaced
-by the partials landing in one device buffer.  With one shard the step is a single
-``mla_decode`` call and no merge.
+by the partials landing in one device buffer.  The shards run side by side in one
+``mla_decode_shards`` launch (their pools are consecutive slices of one cache and their
+block-table rows are offset into it), as the ranks of a DCP group run at the same time;
+with ``batched = False`` each shard is its own ``mla_decode`` call.  With one shard the
+step is a single ``mla_decode`` call and no merge.
 """
 from __future__ import annotations
 
@@ -13,14 +16,14 @@ from typing import List, Optional
 
 import torch
 
-from . import alloc_workspace, lse_merge, mla_decode
+from . import alloc_workspace, lse_merge, mla_decode, mla_decode_shards
 from .dcp import build_shard_pool, local_seq_lens
 
 
 class DcpDecodeStep:
     def __init__(self, q: torch.Tensor, block_table: torch.Tensor, G: torch.Tensor,
                  pools: List[torch.Tensor], seq_lens: List[torch.Tensor], q_len: int,
-                 scale: float, lse_base_e: bool):
+                 scale: float, lse_base_e: bool, pool_all: Optional[torch.Tensor] = None):
         self.q = q
         self.block_table = block_table
         self.cp = len(pools)
@@ -37,7 +40,19 @@ class DcpDecodeStep:
         self.lses = torch.empty(self.cp, self.T, H, dtype=torch.float32, device=dev)
         self.out = torch.empty(self.T, H, 512, dtype=torch.bfloat16, device=dev)
         self.out_lse = torch.empty(self.T, H, dtype=torch.float32, device=dev)
-        self.workspace = alloc_workspace(B, H, q_len, dev)
+        self.batched = self.cp > 1
+        if self.cp > 1:
+            # all shards' pages in one cache; shard r's block-table rows point into its slice
+            self.pool_all = pool_all if pool_all is not None else torch.cat(pools)
+            rows, base = [], 0
+            for r, pool in enumerate(pools):
+                nb = pool.shape[0]
+                ok = (block_table >= 0) & (block_table < nb)
+                rows.append(torch.where(ok, block_table + base, torch.full_like(block_table, -1)))
+                base += nb
+            self.block_table_all = torch.cat(rows).contiguous()
+            self.seq_lens_all = torch.cat(seq_lens).contiguous()
+        self.workspace = alloc_workspace(self.cp * B, H, q_len, dev)
 
     @classmethod
     def from_workload(cls, w, device: str = "cuda") -> "DcpDecodeStep":
@@ -49,21 +64,29 @@ class DcpDecodeStep:
         q = w.q.to(dev)
         kvg = w.kv_global.to(dev)
         bt = w.block_table.to(dev)
+        pool_all = synth.poisoned_pool(w.cp * w.num_blocks, w.bs, dev)
         pools, sls = [], []
         for r in range(w.cp):
-            pool = synth.poisoned_pool(w.num_blocks, w.bs, dev)
+            pool = pool_all[r * w.num_blocks:(r + 1) * w.num_blocks]
             build_shard_pool(pool, kvg, w.kv_offsets, w.G.tolist(), bt, w.cp, r)
             pools.append(pool)
             sls.append(local_seq_lens(w.G, w.cp, r).to(dev))
         del kvg
-        return cls(q, bt, w.G, pools, sls, w.q_len, w.scale, w.base_e)
+        return cls(q, bt, w.G, pools, sls, w.q_len, w.scale, w.base_e, pool_all=pool_all)
 
     def kernel_launches_per_step(self) -> int:
         """Kernels one step launches: per shard the split-KV decode (+ its combine when
         the workspace allows splits), plus the cross-shard merge when cp > 1."""
         from . import workspace_size
         split = 1 if workspace_size(self.B, self.H, self.q_len) > 0 else 0
-        return self.cp * (1 + split) + (1 if self.cp > 1 else 0)
+        calls = 1 if (self.cp == 1 or self.batched) else self.cp
+        return calls * (1 + split) + (1 if self.cp > 1 else 0)
+
+    def input_tensors(self) -> List[torch.Tensor]:
+        """The per-step device inputs ``run`` reads besides q (block tables, lengths)."""
+        if self.cp > 1 and self.batched:
+            return [self.block_table_all, self.seq_lens_all, self.gseq]
+        return [self.block_table, *self.seq_lens, self.gseq]
 
     def run(self, stream=None, q: Optional[torch.Tensor] = None):
         q = self.q if q is None else q
@@ -71,6 +94,14 @@ class DcpDecodeStep:
             mla_decode(q, self.pools[0], self.block_table, self.seq_lens[0], self.gseq,
                        self.q_len, 1, 0, self.scale, out=self.out, lse=self.out_lse,
                        lse_base_e=self.lse_base_e, workspace=self.workspace, stream=stream)
+            return self.out, self.out_lse
+        if self.batched:
+            mla_decode_shards(q, self.pool_all, self.block_table_all, self.seq_lens_all,
+                              self.gseq, self.q_len, self.cp, self.scale, out=self.partials,
+                              lse=self.lses, lse_base_e=self.lse_base_e,
+                              workspace=self.workspace, stream=stream)
+            lse_merge(self.partials, self.lses, out=self.out, out_lse=self.out_lse,
+                      lse_base_e=self.lse_base_e, stream=stream)
             return self.out, self.out_lse
         for r in range(self.cp):
             mla_decode(q, self.pools[r], self.block_table, self.seq_lens[r], self.gseq,

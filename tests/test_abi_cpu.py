@@ -89,6 +89,39 @@ def test_decode_rejects(lib, kw, code):
     assert lib.mla_last_error().decode()
 
 
+def _decode_shards(lib, **kw):
+    a = dict(q=16, kv=16, bt=16, bt_stride=4, seq=16, gseq=16, B=1, H=16, q_len=1, bs=16,
+             num_blocks=4, max_blocks=4, n=2, scale=0.1, out=16, lse=16, base_e=1,
+             ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.mla_decode_shards(a["q"], a["kv"], a["bt"], a["bt_stride"], a["seq"], a["gseq"],
+                                 a["B"], a["H"], a["q_len"], a["bs"], a["num_blocks"],
+                                 a["max_blocks"], a["n"], a["scale"], a["out"], a["lse"],
+                                 a["base_e"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=0), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(n=-3), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(gseq=None), _lib.MLA_ERR_INVALID_ARGUMENT),     # several shards need global lengths
+    (dict(B=-1), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(q_len=17), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(max_blocks=5, bt_stride=4), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(scale=float("inf")), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(kv=None), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(out=24), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(B=1 << 20, H=1 << 8, q_len=16, n=16), _lib.MLA_ERR_UNSUPPORTED),  # rows past 2^31
+    (dict(B=20000, n=16), _lib.MLA_ERR_UNSUPPORTED),     # n * B^2 >= 2^32
+])
+def test_decode_shards_rejects(lib, kw, code):
+    assert _decode_shards(lib, **kw) == code
+    assert lib.mla_last_error().decode().startswith("mla_decode_shards")
+
+
+def test_decode_shards_empty_batch_is_noop(lib):
+    assert _decode_shards(lib, B=0, q=None, out=None) == _lib.MLA_OK
+
+
 def test_decode_empty_batch_is_noop(lib):
     assert _decode(lib, B=0, q=None, out=None) == _lib.MLA_OK
 

@@ -156,27 +156,28 @@ def test_lse_merge_skips_nan_partials_of_empty_shards():
 # ---------------------------------------------------------------------------
 # mla_decode: whole workloads at sizes the oracle finishes in seconds
 # ---------------------------------------------------------------------------
-def _gpu_shards(w, with_workspace=True):
+def _gpu_shards(w, with_workspace=True, batched=True):
     step = DcpDecodeStep.from_workload(w, DEV)
+    step.batched = batched and step.cp > 1
     if not with_workspace:
         step.workspace = torch.empty(0, dtype=torch.uint8, device=DEV)
     return step
 
 
-def _check_workload(w, relative=False, with_workspace=True):
-    step = _gpu_shards(w, with_workspace)
+def _check_workload(w, relative=False, with_workspace=True, batched=True):
+    step = _gpu_shards(w, with_workspace, batched)
     out, lse = step.run()
     torch.cuda.synchronize()
     if relative:
-        ro, rl, mo, ml, ra, ma = H.oracle_shards(w, with_abs=True)
+        ro, rl, mo, ml, ra, ma, rd, md = H.oracle_shards(w, with_abs=True)
     else:
         ro, rl, mo, ml = H.oracle_shards(w)
-        ra, ma = [None] * w.cp, None
+        ra, ma, rd, md = [None] * w.cp, None, [None] * w.cp, None
     if w.cp > 1:
         for r in range(w.cp):
             H.compare(step.partials[r], step.lses[r], ro[r], rl[r], relative,
-                      f"{w.name} shard {r}", ra[r])
-    H.compare(out, lse, mo, ml, relative, f"{w.name} merged", ma)
+                      f"{w.name} shard {r}", ra[r], rd[r])
+    H.compare(out, lse, mo, ml, relative, f"{w.name} merged", ma, md)
     assert M.device_status() == 0
 
 
@@ -195,6 +196,47 @@ def test_decode_cp2_full(kernel):
 ])
 def test_decode_reduced_workloads(name, lengths, kernel):
     _check_workload(synth.make_workload(name, lengths=lengths), relative=(name == "long"))
+
+
+@pytest.mark.parametrize("with_workspace", [True, False])
+@pytest.mark.parametrize("name,lengths", [("cp2", None), ("spec", [3000, 1234, 77])])
+def test_decode_shard_by_shard_calls(name, lengths, with_workspace, kernel):
+    # the per-shard entry point (one mla_decode call per rank) against the oracle, as the
+    # layer step runs it with batched = False
+    _check_workload(synth.make_workload(name, lengths=lengths), with_workspace=with_workspace,
+                    batched=False)
+
+
+def test_decode_shards_matches_per_shard_calls(kernel):
+    # one launch over all shards and one call per shard compute the same partials
+    w = synth.make_custom(3, 64, 4, [900, 65, 2100], 64, 4, base_e=False, seed=77)
+    a = _gpu_shards(w, batched=True)
+    a.run()
+    b = _gpu_shards(w, batched=False)
+    b.run()
+    torch.cuda.synchronize()
+    assert M.device_status() == 0
+    ro, rl, _, _ = H.oracle_shards(w)
+    for r in range(w.cp):
+        H.compare(a.partials[r], a.lses[r], ro[r], rl[r], False, f"batched shard {r}")
+        H.compare(b.partials[r], b.lses[r], ro[r], rl[r], False, f"per-shard call {r}")
+    assert (a.partials.float() - b.partials.float()).abs().max().item() <= 2e-2
+    assert (a.lses - b.lses).abs().max().item() <= 1e-3
+
+
+def test_decode_shards_padded_block_table_rows(kernel):
+    # shard r's rows point into slice r of the shared cache; out-of-range page ids stay
+    # out of range (flagged, not read from another shard's slice)
+    w = synth.make_custom(2, 16, 1, [40, 40], 16, 2, seed=12)
+    step = _gpu_shards(w)
+    base = w.num_blocks
+    bt = step.block_table_all.clone()
+    assert int(bt[2:].max()) >= base                     # shard 1 rows are offset
+    step.block_table_all[3, 0] = -5                      # shard 1, request 1, keys 0..15
+    step.run()
+    torch.cuda.synchronize()
+    assert M.device_status() & 1
+    step.block_table_all.copy_(bt)
 
 
 def test_decode_without_workspace_matches(kernel):
@@ -293,19 +335,22 @@ def _sampled_full(name, sample, relative=False):
     torch.cuda.synchronize()
     assert M.device_status() == 0
     get = H.device_row_getter(w)
-    outs, lses, absw = [], [], []
+    outs, lses, absw, dels = [], [], [], []
     idx = [b * w.q_len + i for b, i in sample]
     for r in range(w.cp):
-        o, l, a = H.oracle_sampled_shard(w, sample, r, get, with_abs=True)
+        o, l, a, d = H.oracle_sampled_shard(w, sample, r, get, with_abs=True)
         outs.append(o)
         lses.append(l)
         absw.append(a)
+        dels.append(d)
         if r < 2 and w.cp > 1:
             H.compare(step.partials[r][idx], step.lses[r][idx], o[idx], l[idx], relative,
-                      f"{name} shard {r}", a[idx])
+                      f"{name} shard {r}", a[idx], d[idx])
     mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), w.base_e)
     ma, _ = R.ref_lse_merge(np.stack(absw), np.stack(lses), w.base_e)
-    H.compare(out[idx], lse[idx], mo[idx], ml[idx], relative, f"{name} merged", ma[idx])
+    md = np.max(np.stack(dels), axis=0)
+    H.compare(out[idx], lse[idx], mo[idx], ml[idx], relative, f"{name} merged", ma[idx],
+              md[idx])
     # properties that hold for every row: finite outputs, |out| bounded by max |V|
     assert torch.isfinite(out.float()).all()
     assert torch.isfinite(lse).all()
