@@ -253,9 +253,10 @@ def time_e2e(step, steps, warmup, flush):
 # call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
 # source they were taken on: a changed kernel reports null until it is captured again.
 TRAFFIC = {
-    # decode 21,967,019 B read, combine 11,601,237 B read, no DRAM writes (mean of 3 calls;
+    # the mla_decode_shards call of cp2 (both shards in one launch): decode 41,367,552 B
+    # read + 46,421 B written, combine 12,656,469 B read (mean of 3 calls;
     # profiles/dram_traffic_cp2.md)
-    ("cp2", "04422381a28086dfe44c743695c42168d7f6ae91c2c00f72c1f81f2243567c18"): 33568256,
+    ("cp2", "81f0b307d2c50a113d0144932d88fa1d07815b06160176de0191278e76da191e"): 54070442,
 }
 
 
