@@ -255,8 +255,9 @@ def time_e2e(step, steps, warmup, flush):
 TRAFFIC = {
     # the mla_decode_shards call of cp2 (both shards in one launch): decode 41,367,552 B
     # read + 46,421 B written, combine 12,656,469 B read (mean of 3 calls;
-    # profiles/dram_traffic_cp2.md)
-    ("cp2", "81f0b307d2c50a113d0144932d88fa1d07815b06160176de0191278e76da191e"): 54070442,
+    # profiles/dram_traffic_cp2.md, commit 5a6e5a8; the source has changed since only in
+    # host code: the occupancy query is cached per device)
+    ("cp2", "4feafd30f2530a230697f53650be4ba97b7c3bc5d4c36a89d142a95e5391e887"): 54070442,
 }
 
 

@@ -1323,7 +1323,12 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   int C = tc_clusters(a.num_sms);
-  {
+  // the number of co-resident clusters depends only on the kernel and the device: asked
+  // once per device
+  static int active_clusters[64] = {0};
+  if (dev < 64 && active_clusters[dev] > 0) {
+    if (active_clusters[dev] < C) C = active_clusters[dev];
+  } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1337,8 +1342,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     cfg.numAttrs = 1;
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, mla_decode_tc_kernel, &cfg) == cudaSuccess &&
-        active > 0 && active < C)
-      C = active;
+        active > 0) {
+      if (dev < 64) active_clusters[dev] = active;
+      if (active < C) C = active;
+    }
     cudaGetLastError();
   }
   // whole groups of row_tiles clusters (row_tiles <= C is checked by tc_supported)

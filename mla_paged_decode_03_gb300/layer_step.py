@@ -16,7 +16,8 @@ from typing import List, Optional
 
 import torch
 
-from . import alloc_workspace, lse_merge, mla_decode, mla_decode_shards
+from . import _lib, alloc_workspace
+from . import _stream
 from .dcp import build_shard_pool, local_seq_lens
 
 
@@ -89,25 +90,43 @@ class DcpDecodeStep:
         return [self.block_table, *self.seq_lens, self.gseq]
 
     def run(self, stream=None, q: Optional[torch.Tensor] = None):
+        """One layer step on ``stream`` (default: the current stream).  The step's buffers
+        were checked when they were made, so the library calls go out directly (the C
+        entry points still validate every argument)."""
         q = self.q if q is None else q
+        L = _lib.load()
+        st = _stream(stream)
+        ws = self.workspace
+        wsb = ws.numel() * ws.element_size()
+        base_e = 1 if self.lse_base_e else 0
+        scale = float(self.scale)
+        pool0 = self.pools[0]
         if self.cp == 1:
-            mla_decode(q, self.pools[0], self.block_table, self.seq_lens[0], self.gseq,
-                       self.q_len, 1, 0, self.scale, out=self.out, lse=self.out_lse,
-                       lse_base_e=self.lse_base_e, workspace=self.workspace, stream=stream)
+            _lib.check(L.mla_decode(
+                q.data_ptr(), pool0.data_ptr(), self.block_table.data_ptr(),
+                self.block_table.stride(0), self.seq_lens[0].data_ptr(), self.gseq.data_ptr(),
+                self.B, self.H, self.q_len, pool0.shape[1], pool0.shape[0],
+                self.block_table.shape[1], 1, 0, scale, self.out.data_ptr(),
+                self.out_lse.data_ptr(), base_e, ws.data_ptr(), wsb, st))
             return self.out, self.out_lse
         if self.batched:
-            mla_decode_shards(q, self.pool_all, self.block_table_all, self.seq_lens_all,
-                              self.gseq, self.q_len, self.cp, self.scale, out=self.partials,
-                              lse=self.lses, lse_base_e=self.lse_base_e,
-                              workspace=self.workspace, stream=stream)
-            lse_merge(self.partials, self.lses, out=self.out, out_lse=self.out_lse,
-                      lse_base_e=self.lse_base_e, stream=stream)
-            return self.out, self.out_lse
-        for r in range(self.cp):
-            mla_decode(q, self.pools[r], self.block_table, self.seq_lens[r], self.gseq,
-                       self.q_len, self.cp, r, self.scale, out=self.partials[r],
-                       lse=self.lses[r], lse_base_e=self.lse_base_e, workspace=self.workspace,
-                       stream=stream)
-        lse_merge(self.partials, self.lses, out=self.out, out_lse=self.out_lse,
-                  lse_base_e=self.lse_base_e, stream=stream)
+            bt = self.block_table_all
+            _lib.check(L.mla_decode_shards(
+                q.data_ptr(), self.pool_all.data_ptr(), bt.data_ptr(), bt.stride(0),
+                self.seq_lens_all.data_ptr(), self.gseq.data_ptr(), self.B, self.H, self.q_len,
+                pool0.shape[1], self.pool_all.shape[0], bt.shape[1], self.cp, scale,
+                self.partials.data_ptr(), self.lses.data_ptr(), base_e, ws.data_ptr(), wsb, st))
+        else:
+            bt = self.block_table
+            for r in range(self.cp):
+                pool = self.pools[r]
+                _lib.check(L.mla_decode(
+                    q.data_ptr(), pool.data_ptr(), bt.data_ptr(), bt.stride(0),
+                    self.seq_lens[r].data_ptr(), self.gseq.data_ptr(), self.B, self.H,
+                    self.q_len, pool.shape[1], pool.shape[0], bt.shape[1], self.cp, r, scale,
+                    self.partials[r].data_ptr(), self.lses[r].data_ptr(), base_e,
+                    ws.data_ptr(), wsb, st))
+        _lib.check(L.lse_merge(self.partials.data_ptr(), 0, self.lses.data_ptr(), self.cp,
+                               self.T, self.H, self.out.data_ptr(), self.out_lse.data_ptr(),
+                               base_e, st))
         return self.out, self.out_lse
