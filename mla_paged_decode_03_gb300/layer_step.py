@@ -21,6 +21,19 @@ from . import _stream
 from .dcp import build_shard_pool, local_seq_lens
 
 
+def shard_major_block_table(block_table: torch.Tensor, pool_blocks: List[int]) -> torch.Tensor:
+    """Block-table rows of every shard over one cache that holds the shards' pools back to
+    back (shard r's pool starts after those of shards 0..r-1): row r*B + b is request b's
+    row with its page ids offset into shard r's slice.  An id outside [0, pool_blocks[r])
+    becomes -1, so that it stays out of range (flagged, not read from another slice)."""
+    rows, base = [], 0
+    for nb in pool_blocks:
+        ok = (block_table >= 0) & (block_table < nb)
+        rows.append(torch.where(ok, block_table + base, torch.full_like(block_table, -1)))
+        base += nb
+    return torch.cat(rows).contiguous()
+
+
 class DcpDecodeStep:
     def __init__(self, q: torch.Tensor, block_table: torch.Tensor, G: torch.Tensor,
                  pools: List[torch.Tensor], seq_lens: List[torch.Tensor], q_len: int,
@@ -45,13 +58,8 @@ class DcpDecodeStep:
         if self.cp > 1:
             # all shards' pages in one cache; shard r's block-table rows point into its slice
             self.pool_all = pool_all if pool_all is not None else torch.cat(pools)
-            rows, base = [], 0
-            for r, pool in enumerate(pools):
-                nb = pool.shape[0]
-                ok = (block_table >= 0) & (block_table < nb)
-                rows.append(torch.where(ok, block_table + base, torch.full_like(block_table, -1)))
-                base += nb
-            self.block_table_all = torch.cat(rows).contiguous()
+            self.block_table_all = shard_major_block_table(block_table,
+                                                           [p.shape[0] for p in pools])
             self.seq_lens_all = torch.cat(seq_lens).contiguous()
         self.workspace = alloc_workspace(self.cp * B, H, q_len, dev)
 
