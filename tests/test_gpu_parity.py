@@ -224,6 +224,28 @@ def test_decode_shards_matches_per_shard_calls(kernel):
     assert (a.lses - b.lses).abs().max().item() <= 1e-3
 
 
+def test_decode_shards_python_wrapper_and_one_shard(kernel):
+    # the wrapper's own allocations give the layer step's partials bit for bit (the kernel
+    # is deterministic), and one shard through mla_decode_shards is mla_decode
+    w = synth.make_custom(3, 64, 2, [700, 64, 1300], 64, 2, base_e=True, seed=21)
+    step = _gpu_shards(w)
+    step.run()
+    out, lse = M.mla_decode_shards(step.q, step.pool_all, step.block_table_all,
+                                   step.seq_lens_all, step.gseq, step.q_len, step.cp,
+                                   step.scale, lse_base_e=step.lse_base_e)
+    torch.cuda.synchronize()
+    assert out.shape == step.partials.shape and lse.shape == step.lses.shape
+    assert torch.equal(out, step.partials) and torch.equal(lse, step.lses)
+    w1 = synth.make_custom(2, 128, 1, [900, 2049], 64, 1, base_e=True, seed=22)
+    s1 = _gpu_shards(w1)
+    o1, l1 = s1.run()
+    o2, l2 = M.mla_decode_shards(s1.q, s1.pools[0], s1.block_table, s1.seq_lens[0], s1.gseq,
+                                 s1.q_len, 1, s1.scale, lse_base_e=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o2[0], o1) and torch.equal(l2[0], l1)
+    assert M.device_status() == 0
+
+
 def test_decode_shards_padded_block_table_rows(kernel):
     # shard r's rows point into slice r of the shared cache; out-of-range page ids stay
     # out of range (flagged, not read from another shard's slice)
