@@ -15,5 +15,7 @@ from .mla_ref import (  # noqa: F401
     ref_lse_merge,
     ref_mla_decode,
     ref_mla_decode_global,
+    ref_owned_positions,
     ref_row_global_prefix,
+    ref_scatter_kv,
 )

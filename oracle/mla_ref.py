@@ -37,16 +37,29 @@ LN2 = math.log(2.0)
 # ---------------------------------------------------------------------------
 # Visible lengths
 # ---------------------------------------------------------------------------
-def ref_row_global_prefix(G, q_len: int) -> np.ndarray:
+def ref_row_global_prefix(G, q_len: int, causal: bool = True) -> np.ndarray:
     """Global visible prefix of each row of a q_len query block.
 
     [#52188] section "关键源码片段", flashinfer_mla.py ``_prepare_flattened_decode_metadata``:
-    row r of the block sees dcp_tot_seq_lens - (query_len - 1 - r), clamped at 0.
-    Returns int64 [..., q_len].
+    in the causal branch row r of the block sees dcp_tot_seq_lens - (query_len - 1 - r),
+    clamped at 0; in the non-causal branch (a DSpark draft block) every row sees the
+    same context, the request's whole length.  Returns int64 [..., q_len].
     """
     G = np.asarray(G, dtype=np.int64)
+    if not causal:
+        return np.repeat(G[..., None], q_len, axis=-1)
     offs = np.arange(q_len - 1, -1, -1, dtype=np.int64)
     return np.maximum(G[..., None] - offs, 0)
+
+
+def ref_owned_positions(G_row: int, cp: int, rank: int, interleave: int = 1) -> np.ndarray:
+    """Global positions g < G_row that shard ``rank`` holds, in increasing order: the
+    sequence is cut into segments of ``interleave`` positions dealt round-robin to the
+    cp ranks, so g belongs to rank (g // interleave) mod cp ([#52188] section
+    "关键源码片段", cp_local_slot: the segment number modulo CP_SIZE decides the owner).
+    The k-th of them is the shard's local position k."""
+    g = np.arange(int(G_row), dtype=np.int64)
+    return g[(g // interleave) % cp == rank]
 
 
 def ref_local_len(G_row, cp: int, rank: int, interleave: int = 1) -> np.ndarray:
@@ -102,6 +115,27 @@ def ref_cp_local_slot(positions, block_table, block_size: int, cp_size: int, cp_
     return out
 
 
+def ref_scatter_kv(pool, positions, kv_new, block_table, block_size: int, cp_size: int,
+                   cp_rank: int, interleave: int = 1) -> np.ndarray:
+    """Writes new KV rows into shard ``cp_rank``'s paged pool: row kv_new[b, n] goes to
+    slot ref_cp_local_slot(positions)[b, n] when this rank owns that position, and
+    nowhere otherwise ([#52188] section "实现拆解" step 4: the draft inputs apply
+    cp_local_slot to their context and query slots, with the page of a position taken
+    from block_table[pos // (block_size * CP_SIZE)], so that a rank never writes slots
+    another rank is responsible for).  pool [num_blocks, block_size, D] is copied, not
+    changed; the copy is returned."""
+    out = np.array(pool, dtype=np.float64, copy=True)
+    flat = out.reshape(-1, out.shape[-1])
+    slots = ref_cp_local_slot(positions, block_table, block_size, cp_size, cp_rank, interleave)
+    new = np.asarray(kv_new, dtype=np.float64)
+    for b in range(slots.shape[0]):
+        for n in range(slots.shape[1]):
+            sl = int(slots[b, n])
+            if sl != PAD_SLOT_ID:
+                flat[sl] = new[b, n]
+    return out
+
+
 def ref_build_pool(kv_rows: Sequence[np.ndarray], block_table, block_size: int, cp: int,
                    rank: int, num_blocks: int, interleave: int = 1) -> np.ndarray:
     """Shard ``rank``'s paged pool [num_blocks, block_size, D]: every global row g of
@@ -134,7 +168,7 @@ def _softmax_attend(q_rows: np.ndarray, keys: np.ndarray, scale: float):
 
 
 def ref_abs_weighted(q, kv_rows, G, q_len: int, cp_world: int, cp_rank: int, scale: float,
-                     rows=None, row_getter=None):
+                     rows=None, row_getter=None, interleave: int = 1, causal: bool = True):
     """Error scale of a softmax-weighted sum, not a result: sum_l softmax(s)_l |V_l| per
     (row, head, dim) over the keys shard ``cp_rank`` holds (same visibility as
     ref_mla_decode_global).  A kernel that rounds the softmax weights to bf16 (8
@@ -147,8 +181,8 @@ def ref_abs_weighted(q, kv_rows, G, q_len: int, cp_world: int, cp_rank: int, sca
     out = np.zeros((B * q_len, H, D_V), dtype=np.float64)
     todo = rows if rows is not None else [(b, i) for b in range(B) for i in range(q_len)]
     for b, i in todo:
-        Gi = int(ref_row_global_prefix(G[b], q_len)[i])
-        idx = np.arange(cp_rank, Gi, cp_world, dtype=np.int64)
+        Gi = int(ref_row_global_prefix(G[b], q_len, causal)[i])
+        idx = ref_owned_positions(Gi, cp_world, cp_rank, interleave)
         if idx.size == 0:
             continue
         keys = (row_getter(b, idx) if row_getter is not None
@@ -173,26 +207,30 @@ def ref_gather_pages(kv_cache, block_table_row, L: int) -> np.ndarray:
 
 def ref_mla_decode(q, kv_cache, block_table, seq_lens, causal_seqlens_global, q_len: int,
                    cp_world: int, cp_rank: int, scale: float, lse_base_e: bool = True,
-                   rows: Optional[Sequence[tuple]] = None):
+                   rows: Optional[Sequence[tuple]] = None, interleave: int = 1,
+                   causal: bool = True):
     """One shard's partial MLA decode over its paged latent cache.
 
     q [B, q_len, H, 576]; kv_cache [num_blocks, block_size, 576]; block_table [B, *];
     seq_lens [B] shard-local counts; causal_seqlens_global [B] (None only when
-    cp_world == 1, then seq_lens is the global length).
-    Row i of request b sees global prefix G_i ([#52188] snippet), of which this shard
-    holds L_i = min(seq_lens[b], local_len(G_i)) ([#54012] section "实现拆解" step 3: the
-    kernel masks by global position with cp_world/cp_rank); interleave is 1 ([#54012]
-    section "关键源码片段", builder init).  Returns out [B*q_len, H, 512] and lse
-    [B*q_len, H] in base e, or base 2 when lse_base_e is False ([#48180] section
-    "实现拆解" step 1: LSE returned in log2).  ``rows`` limits the work to the listed
-    (b, i) pairs; the other outputs stay 0 / -inf.
+    cp_world == 1 or the block is non-causal).
+    Causal: row i of request b sees global prefix G_i ([#52188] snippet), of which this
+    shard holds L_i = min(seq_lens[b], local_len(G_i)) under round-robin segments of
+    ``interleave`` positions ([#52188] snippet: span = cp * interleave, remainder
+    clamp; [#54012] section "实现拆解" step 3: the kernel masks by global position with
+    cp_world/cp_rank).  Non-causal (a DSpark draft block, [#52188] snippet's other
+    branch: seq_lens repeated per query row): every row sees the shard's whole local
+    sequence, L_i = seq_lens[b].  Returns out [B*q_len, H, 512] and lse [B*q_len, H]
+    in base e, or base 2 when lse_base_e is False ([#48180] section "实现拆解" step 1:
+    LSE returned in log2).  ``rows`` limits the work to the listed (b, i) pairs; the
+    other outputs stay 0 / -inf.
     """
     q = np.asarray(q)
     B, ql, H, D = q.shape
     assert ql == q_len
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     if causal_seqlens_global is None:
-        if cp_world != 1:
+        if cp_world != 1 and causal:
             raise ValueError("causal_seqlens_global is required when cp_world > 1")
         G = seq_lens
     else:
@@ -201,8 +239,11 @@ def ref_mla_decode(q, kv_cache, block_table, seq_lens, causal_seqlens_global, q_
     lse = np.full((B * q_len, H), -np.inf, dtype=np.float64)
     todo = rows if rows is not None else [(b, i) for b in range(B) for i in range(q_len)]
     for b, i in todo:
-        Gi = int(ref_row_global_prefix(G[b], q_len)[i])
-        Li = min(int(seq_lens[b]), int(ref_local_len(Gi, cp_world, cp_rank, 1)))
+        if causal:
+            Gi = int(ref_row_global_prefix(G[b], q_len)[i])
+            Li = min(int(seq_lens[b]), int(ref_local_len(Gi, cp_world, cp_rank, interleave)))
+        else:
+            Li = int(seq_lens[b])
         if Li == 0:
             continue
         keys = ref_gather_pages(kv_cache, np.asarray(block_table)[b], Li)
@@ -215,10 +256,12 @@ def ref_mla_decode(q, kv_cache, block_table, seq_lens, causal_seqlens_global, q_
 def ref_mla_decode_global(q, kv_rows: Sequence[np.ndarray], G, q_len: int, cp_world: int,
                           cp_rank: int, scale: float, lse_base_e: bool = True,
                           rows: Optional[Sequence[tuple]] = None,
-                          row_getter: Optional[Callable] = None):
+                          row_getter: Optional[Callable] = None, interleave: int = 1,
+                          causal: bool = True):
     """The same shard result stated on global positions, with no pages: shard ``cp_rank``
-    holds global position g iff g mod cp_world == cp_rank (round-robin, interleave 1),
-    and row i sees g < G_i.  ``row_getter(b, idx)`` may supply rows lazily (large cases).
+    holds global position g iff (g // interleave) mod cp_world == cp_rank, and row i
+    sees g < G_i (causal) or g < G_b (non-causal).  ``row_getter(b, idx)`` may supply
+    rows lazily (large cases).
     """
     q = np.asarray(q)
     B, ql, H, D = q.shape
@@ -227,8 +270,8 @@ def ref_mla_decode_global(q, kv_rows: Sequence[np.ndarray], G, q_len: int, cp_wo
     lse = np.full((B * q_len, H), -np.inf, dtype=np.float64)
     todo = rows if rows is not None else [(b, i) for b in range(B) for i in range(q_len)]
     for b, i in todo:
-        Gi = int(ref_row_global_prefix(G[b], q_len)[i])
-        idx = np.arange(cp_rank, Gi, cp_world, dtype=np.int64)
+        Gi = int(ref_row_global_prefix(G[b], q_len, causal)[i])
+        idx = ref_owned_positions(Gi, cp_world, cp_rank, interleave)
         if idx.size == 0:
             continue
         keys = (row_getter(b, idx) if row_getter is not None
@@ -242,10 +285,12 @@ def ref_mla_decode_global(q, kv_rows: Sequence[np.ndarray], G, q_len: int, cp_wo
 
 def ref_attention_global(q, kv_rows: Sequence[np.ndarray], G, q_len: int, scale: float,
                          rows: Optional[Sequence[tuple]] = None,
-                         row_getter: Optional[Callable] = None):
+                         row_getter: Optional[Callable] = None, causal: bool = True):
     """Unsharded, unpaged ground truth: row i of request b attends to global rows
-    g < G_b - (q_len - 1 - i).  Returns (out, lse_e)."""
-    return ref_mla_decode_global(q, kv_rows, G, q_len, 1, 0, scale, True, rows, row_getter)
+    g < G_b - (q_len - 1 - i), or g < G_b when the block is non-causal.
+    Returns (out, lse_e)."""
+    return ref_mla_decode_global(q, kv_rows, G, q_len, 1, 0, scale, True, rows, row_getter,
+                                 1, causal)
 
 
 # ---------------------------------------------------------------------------

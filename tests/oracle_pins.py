@@ -358,7 +358,166 @@ def check_abs_weighted_closed_form():
         assert np.max(np.abs(o - a)) < 1e-12
 
 
-ALL_CHECKS = [check_slot_golden, check_local_len_golden, check_local_len_bruteforce,
+def _sdpa_unmasked(q_np, rows, G, scale):
+    """torch float64 SDPA with no mask (every query row sees all G[b] keys), MQA
+    broadcast over heads; returns (out, lse) rows ordered (b, i)."""
+    outs, lses = [], []
+    B, q_len, H, D = q_np.shape
+    for b in range(B):
+        K = torch.from_numpy(np.asarray(rows[b][:G[b]], dtype=np.float64))
+        Qh = torch.from_numpy(np.asarray(q_np[b], dtype=np.float64)).permute(1, 0, 2)[None]
+        Kh = K[None, None].expand(1, H, G[b], D)
+        Vh = K[None, None, :, :512].expand(1, H, G[b], 512)
+        o = torch.nn.functional.scaled_dot_product_attention(Qh, Kh, Vh, scale=scale)
+        lse = torch.logsumexp((Qh @ Kh.transpose(-1, -2)) * scale, dim=-1)
+        outs.append(o[0].permute(1, 0, 2).numpy())
+        lses.append(lse[0].permute(1, 0).numpy())
+    return np.concatenate(outs, 0), np.concatenate(lses, 0)
+
+
+def check_noncausal_vs_sdpa():
+    """A non-causal block (DSpark draft): every row sees the request's whole context.
+    With one shard that is unmasked attention (library SDPA, float64), and each row
+    equals an ordinary single-token decode of that row's query."""
+    scale = 1.0 / math.sqrt(192.0)
+    for seed, (B, H, q_len, G, bs) in enumerate([(2, 4, 3, (37, 130), 16),
+                                                 (3, 2, 4, (1, 64, 65), 8)]):
+        q, rows = make_small_case(100 + seed, B, H, q_len, G, bs)
+        ppr = max((n + bs - 1) // bs for n in G)
+        bt, nb = make_block_table(100 + seed, B, ppr)
+        pool = R.ref_build_pool(rows, bt, bs, 1, 0, nb)
+        Ga = np.array(G)
+        out, lse = R.ref_mla_decode(q, pool, bt, Ga, None, q_len, 1, 0, scale, True,
+                                    causal=False)
+        ro, rl = _sdpa_unmasked(q, rows, list(G), scale)
+        assert np.max(np.abs(out - ro)) < 1e-12, np.max(np.abs(out - ro))
+        assert np.max(np.abs(lse - rl)) < 1e-12
+        for i in range(q_len):
+            o1, l1 = R.ref_mla_decode(q[:, i:i + 1], pool, bt, Ga, None, 1, 1, 0, scale, True)
+            assert np.array_equal(o1, out[i::q_len]) and np.array_equal(l1, lse[i::q_len])
+
+
+def check_noncausal_merge_equals_unsharded():
+    """Non-causal shards (each row reads the shard's whole local sequence, seq_lens),
+    merged through their LSEs, equal unmasked attention over the global sequence."""
+    scale = 0.09
+    for seed, (B, H, q_len, G, bs, cp, il) in enumerate([
+            (2, 3, 3, (29, 50), 4, 3, 1), (2, 2, 4, (7, 66), 8, 2, 4), (1, 2, 2, (40,), 4, 8, 1)]):
+        q, rows, bt, nb = _shard_inputs(200 + seed, B, H, q_len, G, bs, cp)
+        Ga = np.array(G)
+        outs, lses = [], []
+        for rank in range(cp):
+            pool = R.ref_build_pool(rows, bt, bs, cp, rank, nb, il)
+            sl = R.ref_local_len(Ga, cp, rank, il)
+            o, l = R.ref_mla_decode(q, pool, bt, sl, None, q_len, cp, rank, scale, True,
+                                    interleave=il, causal=False)
+            outs.append(o)
+            lses.append(l)
+            g = R.ref_mla_decode_global(q, rows, Ga, q_len, cp, rank, scale, True,
+                                        interleave=il, causal=False)
+            assert np.max(np.abs(o - g[0])) < 1e-12 and np.array_equal(l, g[1])
+        mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), True)
+        ro, rl = _sdpa_unmasked(q, rows, list(G), scale)
+        assert np.max(np.abs(mo - ro)) < 1e-12, np.max(np.abs(mo - ro))
+        assert np.max(np.abs(ml - rl)) < 1e-12
+        go, gl = R.ref_attention_global(q, rows, Ga, q_len, scale, causal=False)
+        assert np.max(np.abs(go - ro)) < 1e-12 and np.max(np.abs(gl - rl)) < 1e-12
+
+
+def check_interleave_merge_equals_unsharded():
+    """Causal shards under round-robin segments of ``interleave`` positions (pools laid
+    out by the slot mapping with the same interleave), merged, equal causal attention
+    over the unsharded sequence (library SDPA with a position mask)."""
+    scale = 1.0 / math.sqrt(192.0)
+    for seed, (B, H, q_len, G, bs, cp, il) in enumerate([
+            (2, 3, 3, (29, 70), 4, 2, 2), (2, 2, 4, (9, 100), 8, 3, 4),
+            (1, 2, 2, (66,), 6, 2, 3), (2, 2, 1, (5, 48), 16, 4, 16)]):
+        q, rows, bt, nb = _shard_inputs(300 + seed, B, H, q_len, G, bs, cp)
+        Ga = np.array(G)
+        outs, lses = [], []
+        for rank in range(cp):
+            pool = R.ref_build_pool(rows, bt, bs, cp, rank, nb, il)
+            sl = R.ref_local_len(Ga, cp, rank, il)
+            o, l = R.ref_mla_decode(q, pool, bt, sl, Ga, q_len, cp, rank, scale, True,
+                                    interleave=il)
+            outs.append(o)
+            lses.append(l)
+            g = R.ref_mla_decode_global(q, rows, Ga, q_len, cp, rank, scale, True,
+                                        interleave=il)
+            assert np.max(np.abs(o - g[0])) < 1e-12 and np.array_equal(l, g[1])
+        mo, ml = R.ref_lse_merge(np.stack(outs), np.stack(lses), True)
+        ro, rl = _sdpa_reference(q, rows, list(G), q_len, scale)
+        assert np.max(np.abs(mo - ro)) < 1e-12, np.max(np.abs(mo - ro))
+        assert np.max(np.abs(ml - rl)) < 1e-12
+
+
+def check_owned_positions():
+    """The positions a shard holds, enumerated, number ref_local_len's closed form; the
+    shards partition the sequence; and the k-th held position is the shard's local
+    position k: the slot mapping puts it at page block_table[k // bs], offset k % bs."""
+    rng = np.random.default_rng(8)
+    for cp, il, bs in [(1, 1, 4), (2, 1, 4), (3, 2, 4), (4, 4, 8), (8, 1, 16), (2, 3, 6)]:
+        nvb = 4
+        bt = rng.permutation(40)[:nvb].reshape(1, nvb)
+        G = nvb * bs * cp
+        seen = np.zeros(G, dtype=int)
+        for rank in range(cp):
+            own = R.ref_owned_positions(G, cp, rank, il)
+            seen[own] += 1
+            for Gp in range(0, G + 1, 3):
+                assert len(R.ref_owned_positions(Gp, cp, rank, il)) == \
+                    int(R.ref_local_len(Gp, cp, rank, il))
+            slots = R.ref_cp_local_slot(own.reshape(1, -1), bt, bs, cp, rank, il)[0]
+            k = np.arange(own.size)
+            assert np.array_equal(slots, bt[0, k // bs] * bs + k % bs), (cp, il, bs, rank)
+        assert np.all(seen == 1)
+
+
+def check_scatter_then_decode():
+    """New KV rows scattered into each shard's pool through the slot mapping: context in
+    one call, then a draft block whose rejected tail (negative positions) is skipped.
+    Every slot another shard owns stays untouched (NaN), and decoding the pools gives the
+    global-position formulation over the accepted rows."""
+    scale = 0.08
+    bs, cp, il = 4, 2, 2
+    B, H, q_len = 2, 2, 1
+    G = (22, 37)
+    q, rows = make_small_case(400, B, H, q_len, G, bs)
+    ppr = max(((n + cp - 1) // cp + bs - 1) // bs for n in G) + 1
+    bt, nb = make_block_table(400, B, ppr)
+    acc = (18, 33)                                   # accepted length; the rest rejected
+    for rank in range(cp):
+        pool = np.full((nb, bs, 576), np.nan)
+        Nc = max(acc) - 4
+        pos_c = np.full((B, Nc), -1, dtype=np.int64)
+        kv_c = np.zeros((B, Nc, 576))
+        for b in range(B):
+            n = acc[b] - 4
+            pos_c[b, :n] = np.arange(n)
+            kv_c[b, :n] = rows[b][:n]
+        pool = R.ref_scatter_kv(pool, pos_c, kv_c, bt, bs, cp, rank, il)
+        pos_d = np.full((B, 8), -1, dtype=np.int64)
+        kv_d = np.zeros((B, 8, 576))
+        for b in range(B):
+            base = acc[b] - 4
+            pos_d[b, :4] = base + np.arange(4)                 # accepted draft rows
+            kv_d[b] = rows[b][base:base + 8]                   # rejected rows stay -1
+        pool = R.ref_scatter_kv(pool, pos_d, kv_d, bt, bs, cp, rank, il)
+        want = R.ref_build_pool([r[:a] for r, a in zip(rows, acc)], bt, bs, cp, rank, nb, il)
+        assert np.array_equal(np.isnan(pool), np.isnan(want))
+        fin = ~np.isnan(want)
+        assert np.array_equal(pool[fin], want[fin])
+        Ga = np.array(acc)
+        sl = R.ref_local_len(Ga, cp, rank, il)
+        a = R.ref_mla_decode(q, pool, bt, sl, Ga, q_len, cp, rank, scale, True, interleave=il)
+        g = R.ref_mla_decode_global(q, rows, Ga, q_len, cp, rank, scale, True, interleave=il)
+        assert np.max(np.abs(a[0] - g[0])) < 1e-12 and np.array_equal(a[1], g[1])
+
+
+ALL_CHECKS = [check_noncausal_vs_sdpa, check_noncausal_merge_equals_unsharded,
+              check_interleave_merge_equals_unsharded, check_owned_positions,
+              check_scatter_then_decode,
+              check_slot_golden, check_local_len_golden, check_local_len_bruteforce,
               check_row_prefix_positions, check_slot_bruteforce, check_decode_vs_sdpa,
               check_decode_bruteforce_tiny, check_merge_closed_form, check_lse_bases,
               check_merge_equals_unsharded, check_pool_vs_global_formulation,
