@@ -7,13 +7,17 @@ launch, as the ranks of a DCP group run at the same time) and ``lse_merge`` of t
 partials.  ``per_config[...]["decode_call_us"]`` is that launch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config cp2] [--extra-configs tiny,plain,spec,long]
+                  [--config spec] [--extra-configs tiny,cp2,plain,long] [--slot-only]
 
-The headline workload is ``cp2`` (8 requests, 64 heads, q_len 4, contexts U[1024, 8192],
-block_size 64, 2 shards, base-2 LSE).  Its 42 MB of KV fits in L2, so L2 is flushed
-(a 512 MB write) before every timed step; only the step itself is inside the CUDA-event
-bracket.  The other workloads are timed the same way and reported under
-``per_config``.  ``--impl reference`` times the float64 CPU oracle on the host cores.
+The headline workload is ``spec``, the largest single-GPU workload: 32 requests, 128
+heads, q_len 4, contexts U[8192, 131072], block_size 64, 8 shards, natural-log LSE.
+Its KV (2.6 GB) is far larger than L2; L2 is flushed (a 512 MB write) before every timed
+step anyway, and only the step itself is inside the CUDA-event bracket.  The other
+workloads are timed the same way and reported under ``per_config``; every workload with
+several shards is also timed with one ``mla_decode`` call per shard
+(``<name>_per_shard``), the form a real DCP rank uses, and ``cp_local_slot`` is timed on
+the long workload's 1,048,576 positions (``cp_local_slot_1M``).  ``--impl reference``
+times the float64 CPU oracle on the host cores.
 
 One JSON line is printed by rank 0.  With torchrun (N > 1) every rank runs an
 independent replica on its own GPU (weak scaling; the step has no cross-GPU exchange).
@@ -41,6 +45,8 @@ import torch  # noqa: E402
 
 import synth  # noqa: E402
 
+CONTEXTS = {"tiny": "37, 130", "cp2": "U[1024,8192]", "plain": "32768 each",
+            "spec": "U[8192,131072]", "long": "U[262144,524288], 1% of KV rows x20"}
 METRIC = "MLA paged decode µs/layer-step, KV GB/s & TFLOP/s vs GB300 roofline"
 UNIT = "us/layer-step"
 L2_FLUSH_BYTES = 512 << 20
@@ -149,22 +155,30 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
-def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None):
-    import mla_paged_decode_03_gb300 as m
-    from mla_paged_decode_03_gb300.layer_step import DcpDecodeStep
+def build_step(name, device, batch=None):
+    from step_builder import step_from_workload
 
     w = synth.make_workload(name, device=device, B=batch)
-    step = DcpDecodeStep.from_workload(w, device)
+    step = step_from_workload(w, device)
     del w.kv_global
+    return w, step
+
+
+def time_step(step, steps, warmup, flush, batched):
+    """CUDA-event times of ``steps`` layer steps (after ``warmup`` untimed ones): the whole
+    step, and each decode call in it (one call over all shards when ``batched``, else one
+    per shard)."""
+    import mla_paged_decode_03_gb300 as m
+
+    step.batched = batched and step.cp > 1
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         step.run()
     torch.cuda.synchronize()
     assert m.device_status() == 0
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(step.cp + 2)]
+    ncalls = 1 if (step.cp == 1 or step.batched) else step.cp
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 2)]
           for _ in range(steps)]
-    step_ms, call_ms = [], []
     torch.cuda.synchronize()
     for k in range(steps):
         flush.zero_()
@@ -191,23 +205,67 @@ def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None):
                 e[r + 1].record(stream)
             m.lse_merge(step.partials, step.lses, out=step.out, out_lse=step.out_lse,
                         lse_base_e=step.lse_base_e)
-            e[step.cp + 1].record(stream)
+            e[ncalls + 1].record(stream)
     torch.cuda.synchronize()
-    calls = 1 if (step.cp == 1 or step.batched) else step.cp
+    step_ms, call_ms, merge_ms = [], [], []
     for k in range(steps):
         e = ev[k]
-        last = e[1] if step.cp == 1 else e[calls + 1]
+        last = e[1] if step.cp == 1 else e[ncalls + 1]
         step_ms.append(e[0].elapsed_time(last))
-        for r in range(calls):
+        for r in range(ncalls):
             call_ms.append(e[r].elapsed_time(e[r + 1]))
+        if step.cp > 1:
+            merge_ms.append(e[ncalls].elapsed_time(e[ncalls + 1]))
     assert m.device_status() == 0
-    wk = work(w)
-    res = dict(step_ms=step_ms, call_ms=call_ms, work=wk, w=w, step=step,
-               launches=step.kernel_launches_per_step(),
-               call_shards=step.cp if (step.cp > 1 and step.batched) else 1)
+    return dict(step_ms=step_ms, call_ms=call_ms, merge_ms=merge_ms,
+                launches=step.kernel_launches_per_step(),
+                call_shards=step.cp if (step.cp > 1 and step.batched) else 1)
+
+
+def time_config(name, steps, warmup, device, flush, with_e2e=False, batch=None,
+                per_shard=False):
+    w, step = build_step(name, device, batch)
+    res = time_step(step, steps, warmup, flush, batched=True)
+    res.update(work=work(w), w=w, step=step)
+    if per_shard and step.cp > 1:
+        res["per_shard"] = time_step(step, steps, warmup, flush, batched=False)
+        step.batched = True
     if with_e2e:
         res["e2e"] = time_e2e(step, steps, warmup, flush)
     return res
+
+
+def time_slot(steps, warmup, device, flush):
+    """cp_local_slot over the long workload's 1,048,576 positions (cp_size 8), one call
+    per rank; HBM-bound at 16 B per position (8 in, 8 out)."""
+    import mla_paged_decode_03_gb300 as m
+
+    case = synth.make_workload("long", draw_values=False).slot_cases[0]
+    w_pos = case.positions.to(device)
+    bt = case.block_table.to(device)
+    slots = torch.empty_like(w_pos)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        m.cp_local_slot(w_pos, bt, case.block_size, case.cp_size, 0, case.interleave, slots=slots)
+    torch.cuda.synchronize()
+    times = []
+    for k in range(steps):
+        for rank in range(case.cp_size):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            m.cp_local_slot(w_pos, bt, case.block_size, case.cp_size, rank, case.interleave,
+                            slots=slots)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+    assert m.device_status() == 0
+    n = w_pos.numel()
+    us = statistics.mean(times) * 1e3
+    return dict(us_per_call=us, positions=n, cp_size=case.cp_size,
+                gbs=16.0 * n / (us * 1e-6) / 1e9, bytes_per_position=16,
+                calls=len(times))
 
 
 def time_e2e(step, steps, warmup, flush):
@@ -249,15 +307,11 @@ def time_e2e(step, steps, warmup, flush):
     return dict(ms=statistics.mean(times), h2d=h2d, d2h=d2h)
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum under ncu) of one mla_decode
-# call, summed over the two kernels it launches, keyed by the SHA-256 of the tcgen05 kernel
-# source they were taken on: a changed kernel reports null until it is captured again.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum under ncu) of one decode call
+# of a workload, summed over the two kernels the call launches (decode + split combine),
+# keyed by the SHA-256 of the tcgen05 kernel source they were taken on: a changed kernel
+# reports null until it is captured again.
 TRAFFIC = {
-    # the mla_decode_shards call of cp2 (both shards in one launch): decode 41,367,552 B
-    # read + 46,421 B written, combine 12,656,469 B read (mean of 3 calls;
-    # profiles/dram_traffic_cp2.md, commit 5a6e5a8; the source has changed since only in
-    # host code: the occupancy query is cached per device)
-    ("cp2", "4feafd30f2530a230697f53650be4ba97b7c3bc5d4c36a89d142a95e5391e887"): 54070442,
 }
 
 
@@ -292,26 +346,34 @@ def summarize(res, pk):
                 decode_call_us=call * 1e6,
                 decode_call_tflops=shard_flops / call / 1e12,
                 decode_call_gbs=shard_bytes / call / 1e9,
+                decode_calls_per_step=len(res["call_ms"]) // max(1, len(res["step_ms"])),
+                merge_us=(statistics.mean(res["merge_ms"]) * 1e3 if res.get("merge_ms") else 0.0),
                 kv_gb=wk["kv_bytes"] / 1e9, gflop=wk["flops"] / 1e9,
                 launches_per_step=res["launches"])
 
 
-def cpu_baseline_sample(name, budget_s=12.0):
+def baseline_workload(name):
+    """The workload the CPU baseline samples: the same seeded draws as the GPU arm (drawn
+    on the GPU when there is one, which is quicker for the large workloads)."""
+    return synth.make_workload(name, device="cuda" if torch.cuda.is_available() else "cpu")
+
+
+def cpu_baseline_sample(name, budget_s=12.0, w=None, first=0):
     """Times the float64 oracle on the host cores on a bounded sample of the workload:
-    whole requests (all shards + merge) until ~budget_s of CPU work, scaled to one
-    layer-step by the share of the step's flops the sample covered."""
+    whole requests from ``first`` on (all shards + merge) until ~budget_s of CPU work,
+    scaled to one layer-step by the share of the step's flops the sample covered."""
     import oracle.mla_ref as R
 
-    w = synth.make_workload(name)
+    if w is None:
+        w = synth.make_workload(name)
     wk = work(w)
-    q = w.q.double().numpy()
-    bt = w.block_table.numpy()
+    q = w.q.to("cpu", torch.float64).numpy()
     G = w.G.numpy()
-    order = list(range(w.B))
+    order = [(first + k) % w.B for k in range(w.B)]
     done_flops, elapsed, used = 0.0, 0.0, []
     Gr = _row_prefixes(G, w.q_len)
     for b in order:
-        rows_b = w.rows_of(b).double().numpy()
+        rows_b = w.rows_of(b).to("cpu", torch.float64).numpy()
         t0 = time.perf_counter()
         outs, lses = [], []
         for r in range(w.cp):
@@ -362,13 +424,24 @@ def run_ours(args):
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
+    if args.slot_only:
+        r = time_slot(max(1, args.steps), args.warmup, device, flush)
+        if rank == 0:
+            print(json.dumps({"cp_local_slot_1M": r}))
+        return
+
     per_config = {}
     extra = [c for c in args.extra_configs.split(",") if c and c != args.config]
     for name in extra:
-        r = time_config(name, max(3, args.steps), max(3, args.warmup), device, flush)
+        r = time_config(name, max(3, args.steps), max(3, args.warmup), device, flush,
+                        per_shard=True)
         per_config[name] = summarize(r, pk)
+        if "per_shard" in r:
+            per_config[name + "_per_shard"] = summarize(dict(r["per_shard"], work=r["work"]), pk)
         del r
         torch.cuda.empty_cache()
+    if args.extra_configs:
+        per_config["cp_local_slot_1M"] = time_slot(max(3, args.steps) // 3 + 1, 3, device, flush)
 
     if ws > 1:
         import torch.distributed as dist
@@ -377,11 +450,14 @@ def run_ours(args):
     sampler.start()
     wall0 = time.perf_counter()
     res = time_config(args.config, args.steps, args.warmup, device, flush, with_e2e=True,
-                      batch=args.batch)
+                      batch=args.batch, per_shard=args.batch is None)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     s = summarize(res, pk)
     per_config[args.config] = s
+    if "per_shard" in res:
+        per_config[args.config + "_per_shard"] = summarize(dict(res["per_shard"], work=res["work"]),
+                                                           pk)
     ms = reduce_max(s["us_per_step"] / 1e3, ws, device)
     e2e_ms = reduce_max(res["e2e"]["ms"], ws, device)
     if ws > 1:
@@ -401,15 +477,18 @@ def run_ours(args):
                             "combine in one launch)" if res["call_shards"] > 1 else
                             "mla_decode call (split-KV decode + split combine)"),
                  "peak_source": pk["source"] + " (burst)"})
-    cpu = (cpu_baseline_sample(args.config) if (ws == 1 and not args.no_cpu_baseline
-                                                  and args.batch is None) else None)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline and args.batch is None:
+        del res["step"]
+        torch.cuda.empty_cache()
+        cpu = cpu_baseline_sample(args.config, w=baseline_workload(args.config))
     line = {
         "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.config, "B": res["w"].B, "H": res["w"].H,
                    "q_len": res["w"].q_len, "block_size": res["w"].bs, "shards": res["w"].cp,
-                   "contexts": "U[1024,8192]" if args.config == "cp2" else "see synth",
+                   "contexts": CONTEXTS.get(args.config, "see synth"),
                    "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": (f"replicas{ws}" if ws > 1 else
                                    "single GPU, emulated DCP shards (all shards in one launch)"
@@ -436,13 +515,14 @@ def run_reference(args):
         return
     name = args.config
     budget = float(os.environ.get("REF_SAMPLE_SECONDS", min(8.0, 120.0 / max(1, args.steps))))
+    w = baseline_workload(name)
     vals = []
-    for _ in range(args.warmup):
-        cpu_baseline_sample(name, budget_s=0.5)
+    for k in range(args.warmup):
+        cpu_baseline_sample(name, budget_s=0.5, w=w, first=k)
     last = None
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        last = cpu_baseline_sample(name, budget_s=budget)
+    for k in range(args.steps):
+        last = cpu_baseline_sample(name, budget_s=budget, w=w, first=k)
         vals.append(last["value"])
     wall = time.perf_counter() - t0
     v = statistics.mean(vals)
@@ -464,8 +544,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="cp2", choices=synth.ORDER)
-    ap.add_argument("--extra-configs", default="tiny,plain,spec,long")
+    ap.add_argument("--config", default="spec", choices=synth.ORDER)
+    ap.add_argument("--extra-configs", default="tiny,cp2,plain,long")
+    ap.add_argument("--slot-only", action="store_true",
+                    help="time only cp_local_slot on the 1,048,576-position case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the headline workload's batch (profiling runs only)")

@@ -2,9 +2,12 @@
 
 Thin PyTorch-facing wrappers over the C ABI of ``libmla_decode.so``:
 
-  mla_decode     one shard's partial attention (out, lse) for q_len-row query blocks
-  lse_merge      merge shard partials through their LSEs
-  cp_local_slot  global position -> this rank's KV slot (PAD_SLOT_ID = -1 otherwise)
+  mla_decode             one shard's partial attention (out, lse) for q_len-row query
+                         blocks, causal or not, any round-robin interleave
+  mla_decode_shards      every emulated shard of a step in one launch
+  lse_merge              merge shard partials through their LSEs
+  cp_local_slot          global position -> this rank's KV slot (PAD_SLOT_ID = -1 otherwise)
+  cp_local_slot_scatter  write new KV rows into this rank's pool at those slots
 
 PyTorch provides device memory and the current stream; every step of the computation
 runs in the library's CUDA kernels.  All tensors must live on the current CUDA device.
@@ -22,8 +25,9 @@ from ._lib import PAD_SLOT_ID, MlaError  # noqa: F401
 D_QK = 576
 D_V = 512
 
-__all__ = ["mla_decode", "mla_decode_shards", "lse_merge", "cp_local_slot", "workspace_size", "device_status",
-           "PAD_SLOT_ID", "MlaError", "D_QK", "D_V"]
+__all__ = ["mla_decode", "mla_decode_shards", "lse_merge", "cp_local_slot",
+           "cp_local_slot_scatter", "workspace_size", "device_status", "set_decode_kernel",
+           "set_rescale_budget", "set_wait_limit_ns", "PAD_SLOT_ID", "MlaError", "D_QK", "D_V"]
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -66,14 +70,17 @@ def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tenso
                q_len: int, cp_world: int, cp_rank: int, scale: float,
                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                lse_base_e: bool = True, workspace: Optional[torch.Tensor] = None,
-               return_lse: bool = True, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+               return_lse: bool = True, stream=None, causal: bool = True,
+               interleave: int = 1) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """One shard's partial MLA decode.
 
     q [B, q_len, H, 576] (or [B*q_len, H, 576]) bf16; kv_cache [num_blocks, block_size,
     576] bf16; block_table [B, max_blocks] int32 (row stride may exceed max_blocks);
     seq_lens [B] int32 shard-local counts; causal_seqlens_global [B] int32 global
-    lengths (None only when cp_world == 1).  Returns out [B*q_len, H, 512] bf16 and lse
-    [B*q_len, H] float32 (natural log, or log2 when lse_base_e is False).
+    lengths (None when cp_world == 1 or the block is non-causal).  ``causal`` False: every
+    query row reads the shard's whole local sequence.  ``interleave``: the KV is dealt to
+    the ranks in round-robin segments of that many positions.  Returns out [B*q_len, H,
+    512] bf16 and lse [B*q_len, H] float32 (natural log, or log2 when lse_base_e is False).
     """
     if q.dim() == 3:
         q = q.view(-1, q_len, q.shape[1], q.shape[2])
@@ -104,9 +111,10 @@ def mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tenso
     L = _lib.load()
     rc = L.mla_decode(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                       block_table.stride(0), seq_lens.data_ptr(), _ptr(causal_seqlens_global),
-                      B, H, q_len, kv_cache.shape[1], kv_cache.shape[0], block_table.shape[1],
-                      cp_world, cp_rank, float(scale), out.data_ptr(), _ptr(lse),
-                      1 if lse_base_e else 0, workspace.data_ptr(), ws_bytes, _stream(stream))
+                      B, H, q_len, 1 if causal else 0, kv_cache.shape[1], kv_cache.shape[0],
+                      block_table.shape[1], cp_world, cp_rank, int(interleave), float(scale),
+                      out.data_ptr(), _ptr(lse), 1 if lse_base_e else 0, workspace.data_ptr(),
+                      ws_bytes, _stream(stream))
     _lib.check(rc)
     return out, lse
 
@@ -116,7 +124,8 @@ def mla_decode_shards(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
                       q_len: int, n_shards: int, scale: float,
                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                       lse_base_e: bool = True, workspace: Optional[torch.Tensor] = None,
-                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                      stream=None, causal: bool = True,
+                      interleave: int = 1) -> Tuple[torch.Tensor, torch.Tensor]:
     """Every shard of an emulated context-parallel step in one launch: the result equals
     ``mla_decode`` of shard r (rank r of cp_world = n_shards) for each r.
 
@@ -155,10 +164,11 @@ def mla_decode_shards(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
     L = _lib.load()
     rc = L.mla_decode_shards(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
                              block_table.stride(0), seq_lens.data_ptr(),
-                             _ptr(causal_seqlens_global), B, H, q_len, kv_cache.shape[1],
-                             kv_cache.shape[0], block_table.shape[1], n_shards, float(scale),
-                             out.data_ptr(), lse.data_ptr(), 1 if lse_base_e else 0,
-                             workspace.data_ptr(), ws_bytes, _stream(stream))
+                             _ptr(causal_seqlens_global), B, H, q_len, 1 if causal else 0,
+                             kv_cache.shape[1], kv_cache.shape[0], block_table.shape[1],
+                             n_shards, int(interleave), float(scale), out.data_ptr(),
+                             lse.data_ptr(), 1 if lse_base_e else 0, workspace.data_ptr(),
+                             ws_bytes, _stream(stream))
     _lib.check(rc)
     return out, lse
 
@@ -215,13 +225,72 @@ def cp_local_slot(positions: torch.Tensor, block_table: torch.Tensor, block_size
     return slots
 
 
+def cp_local_slot_scatter(positions: torch.Tensor, kv_new: torch.Tensor,
+                          block_table: torch.Tensor, kv_cache: torch.Tensor, cp_size: int,
+                          cp_rank: int, interleave: int = 1,
+                          slots: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Writes kv_new [B, N, 576] bf16 into kv_cache [num_blocks, block_size, 576] at the
+    slots ``cp_local_slot`` gives positions [B, N] on rank ``cp_rank``; positions the rank
+    does not own (and negative ones) write nothing.  Returns kv_cache."""
+    if positions.dim() == 1:
+        positions = positions.view(1, -1)
+    _need(positions, "positions", torch.int64, 2)
+    B, N = positions.shape
+    _need(kv_new, "kv_new", torch.bfloat16, 3)
+    if tuple(kv_new.shape) != (B, N, D_QK):
+        raise ValueError(f"kv_new must be [B, N, {D_QK}], got {tuple(kv_new.shape)}")
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    if kv_cache.shape[2] != D_QK:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 576]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or not block_table.is_cuda:
+        raise TypeError("block_table must be a 2-D int32 CUDA tensor")
+    if block_table.stride(1) != 1 or block_table.shape[0] != B:
+        raise ValueError("block_table must have one contiguous row per positions row")
+    if slots is not None:
+        _need(slots, "slots", torch.int64, 2)
+    rc = _lib.load().cp_local_slot_scatter(
+        positions.data_ptr(), kv_new.data_ptr(), block_table.data_ptr(), block_table.stride(0),
+        block_table.shape[1], B, N, kv_cache.shape[1], cp_size, cp_rank, interleave,
+        kv_cache.data_ptr(), kv_cache.shape[0], _ptr(slots), _stream(stream))
+    _lib.check(rc)
+    return kv_cache
+
+
 KERNEL_AUTO, KERNEL_MMA, KERNEL_TC = 0, 1, 2
+BUDGET_AUTO, BUDGET_NARROW, BUDGET_WIDE = 0, 1, 2
 
 
 def set_decode_kernel(choice: int) -> int:
     """0 = automatic, 1 = warp-level mma.sync kernel, 2 = tcgen05 kernel where it applies.
     Returns the previous choice."""
     rc = _lib.load().mla_set_decode_kernel(int(choice))
+    if rc < 0:
+        _lib.check(rc)
+    return rc
+
+
+def set_rescale_budget(choice: int) -> int:
+    """Lazy-rescale budget of the tcgen05 kernel: 0 = per call, 1 = narrow, 2 = wide.
+    Returns the previous choice."""
+    rc = _lib.load().mla_set_rescale_budget(int(choice))
+    if rc < 0:
+        _lib.check(rc)
+    return rc
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of every bounded on-chip wait of later launches (0 = default, 2 s).  Returns
+    the previous setting."""
+    rc = _lib.load().mla_set_wait_limit_ns(int(ns))
+    if rc < 0:
+        _lib.check(int(rc))
+    return int(rc)
+
+
+def set_test_stall(on: bool) -> int:
+    """Tests of the timeout path only: make later decode launches wait for an arrival that
+    never comes (the wait runs out after the wait limit).  Returns the previous setting."""
+    rc = _lib.load().mla_set_test_stall(1 if on else 0)
     if rc < 0:
         _lib.check(rc)
     return rc

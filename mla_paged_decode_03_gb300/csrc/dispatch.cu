@@ -1,13 +1,16 @@
-// Kernel choice for mla_decode: the tcgen05 kernel wherever the KV layout allows TMA
-// tiles, the warp-level kernel otherwise.
+// Kernel choice for mla_decode: the tcgen05 kernel wherever the KV layout allows its TMA
+// tiles.  The warp-level kernel runs only when a test selects it (a second, independent
+// GPU implementation to cross-check the first); other layouts are refused by the caller.
+#include <atomic>
+
 #include "internal.h"
 
 namespace mla {
 namespace {
-int g_choice = 0;
+std::atomic<int> g_choice{0};
 }
 
-void set_decode_kernel_choice(int choice) { g_choice = choice; }
+void set_decode_kernel_choice(int choice) { g_choice.store(choice); }
 
 size_t decode_workspace_size(int B, int H, int q_len, int num_sms) {
   const size_t a = tc_workspace_size(B, H, q_len, num_sms);
@@ -16,15 +19,20 @@ size_t decode_workspace_size(int B, int H, int q_len, int num_sms) {
 }
 
 size_t decode_workspace_for(int B, int H, int q_len, int num_sms, int block_size) {
-  const bool tc_bs = block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
-  if (g_choice != 1 && tc_bs) return tc_workspace_size(B, H, q_len, num_sms);
+  if (g_choice != 1 && tc_block_size_ok(block_size)) return tc_workspace_size(B, H, q_len, num_sms);
   return mma_workspace_size(B, H, q_len, num_sms);
+}
+
+DecodeKernel choose_decode_kernel(const DecodeArgs& a) {
+  if (g_choice == 1) return kDecodeMma;
+  return tc_supported(a) ? kDecodeTc : kDecodeNone;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B == 0 || a.H * a.q_len == 0) return cudaSuccess;
-  const bool tc = g_choice == 2 || (g_choice == 0 && tc_supported(a));
-  if (tc && tc_supported(a)) return launch_decode_tc(a, stream);
+  const DecodeKernel k = choose_decode_kernel(a);
+  if (k == kDecodeTc) return launch_decode_tc(a, stream);
+  if (k != kDecodeMma) return cudaErrorNotSupported;
   if (a.shard_B == a.B) return launch_decode_mma(a, stream);
   // several shards in one call: the warp-level kernel takes them one launch each
   const long long rows = (long long)a.shard_B * a.q_len * a.H;

@@ -1,12 +1,17 @@
 // Split-KV paged MLA decode on the warp-level tensor-core path (mma.sync m16n8k16 bf16).
 //
-// What it computes (one shard, interleave 1): query row i of request b sees the global
-// prefix G_i = max(0, G_b - (q_len-1-i)) ("vLLM PR #52188 (DSpark + DCP)" page, section
-// "关键源码片段", _prepare_flattened_decode_metadata), of which this shard holds
-// L_i = min(seq_lens[b], G_i / cp + (G_i % cp > rank)) keys; keys are gathered page by
-// page through the block table; out = softmax(scale * q K^T) V with V = K[:, :512] and
-// lse in base e or 2 ("vLLM PR #54012" page, section "实现拆解" step 3; "vLLM PR #48180"
-// page, section "实现拆解" step 1).
+// What it computes (one shard): query row i of request b sees the global prefix
+// G_i = max(0, G_b - (q_len-1-i)) ("vLLM PR #52188 (DSpark + DCP)" page, section
+// "关键源码片段", _prepare_flattened_decode_metadata), of which this shard holds, under
+// round-robin segments of I positions (span = cp * I),
+// L_i = min(seq_lens[b], G_i / span * I + clamp(G_i % span - rank * I, 0, I)) keys (a
+// non-causal block reads L_i = seq_lens[b] in every row, the snippet's other branch);
+// keys are gathered page by page through the block table; out = softmax(scale * q K^T) V
+// with V = K[:, :512] and lse in base e or 2 ("vLLM PR #54012" page, section "实现拆解"
+// step 3; "vLLM PR #48180" page, section "实现拆解" step 1).
+//
+// This kernel is a cross-check of the tcgen05 kernel: calls run it only when a test
+// selects it (mla_set_decode_kernel).
 //
 // Layout of the work: a CTA of 8 warps takes 64 query rows of one request (rows ordered
 // (q-row i, head h), so a request's q_len*H rows share every key) and one contiguous
@@ -46,6 +51,8 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* gseq;
   int B, H, q_len, bs, num_blocks, max_blocks, cp, rank;
+  int causal, il;
+  long long span;
   int rows;
   int splits;
   float scale_log2;
@@ -101,10 +108,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Keys visible to query row r (ordered (i, h)) of request b on this shard.
 __device__ __forceinline__ int row_bound(const Params& p, int r, long long G, int cap) {
+  if (!p.causal) return cap;
   const int i = r / p.H;
   long long Gi = G - (p.q_len - 1 - i);
   if (Gi < 0) Gi = 0;
-  const long long loc = Gi / p.cp + ((Gi % p.cp) > p.rank ? 1 : 0);
+  long long rem = Gi % p.span - (long long)p.rank * p.il;
+  rem = rem < 0 ? 0 : (rem > p.il ? p.il : rem);
+  const long long loc = Gi / p.span * p.il + rem;
   return (int)(loc < cap ? loc : cap);
 }
 
@@ -373,6 +383,9 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
   p.max_blocks = a.max_blocks;
   p.cp = a.cp_world;
   p.rank = a.cp_rank;
+  p.causal = a.causal ? 1 : 0;
+  p.il = a.interleave;
+  p.span = (long long)a.cp_world * a.interleave;
   p.rows = rows;
   p.splits = splits;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -391,14 +404,12 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
     p.ws_lse = nullptr;
   }
 
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  // the shared-memory attribute is set on every call: this kernel runs only in tests,
+  // and the call is cheap and safe from several host threads at once
+  {
     cudaError_t e = cudaFuncSetAttribute(mla_decode_mma_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
   }
   dim3 grid(splits, (rows + kRows - 1) / kRows, a.B);
   mla_decode_mma_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);

@@ -2,8 +2,11 @@
 //
 // What it computes is the same as the warp-level kernel (mla_decode_mma.cu): query row i
 // of request b sees the global prefix G_i = max(0, G_b - (q_len-1-i)) ("vLLM PR #52188
-// (DSpark + DCP)" page, section "关键源码片段"), this shard holds
-// L_i = min(seq_lens[b], G_i / cp + (G_i % cp > rank)) of those keys, and
+// (DSpark + DCP)" page, section "关键源码片段"), of which this shard holds, under
+// round-robin segments of I positions (span = cp * I),
+// L_i = min(seq_lens[b], G_i / span * I + clamp(G_i % span - rank * I, 0, I)) keys; a
+// non-causal block (the same snippet's other branch, a DSpark draft block) reads the
+// shard's whole local sequence, L_i = seq_lens[b], in every row.
 // out = softmax(scale q K^T) V with V = K[:, :512], lse in base e or 2 ("vLLM PR #54012"
 // page, section "实现拆解" step 3; "vLLM PR #48180" page, section "实现拆解" step 1).
 //
@@ -21,9 +24,10 @@
 //     S; eight softmax warps (two threads per query row, 32 keys each, swapping their row
 //     maxima through shared memory) read S, apply the per-row causal bound,
 //     keep the running max / sum (online softmax in base 2 against a per-row reference
-//     max, set 2^64 above a tile's max and moved only when a tile's max exceeds it by more
-//     than 2^32, so that P <= 2^32 and rescales of O are rare even when a few keys score
-//     far above the rest), and write P (bf16) with the per-row rescale factors into a
+//     max, set a headroom above a tile's max and moved only when a tile's max exceeds it
+//     by more than a threshold, so that P <= 2^threshold and rescales of O are rare even
+//     when a few keys score far above the rest; two budgets are compiled, see Budget),
+//     and write P (bf16) with the per-row rescale factors into a
 //     staging slot, which a copy warp bulk-copies into one of three receive slots of CTA 1.
 //   CTA 1 (the O-CTA) holds O in all 512 TMEM columns.  A TMA warp streams the same keys'
 //     first 512 dims (V) through five half-tile groups; the MMA warp issues 8 MMAs (M=128,
@@ -44,6 +48,10 @@
 // slots past seq_len (which may hold anything) never reach the accumulator.
 #include <math.h>
 #include <stdint.h>
+
+#include <atomic>
+#include <functional>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -71,9 +79,23 @@ constexpr int kPBytes = kM * 128;   // P tile: 128 rows x 64 keys bf16 = 16 KB
 constexpr int kSideBytes = 1024 + 16;         // alpha[128], inv_l[128], flags
 constexpr int kPSlotBytes = 18432;  // P tile + sideband, 1 KB aligned
 constexpr int kPRecv = 3;           // O-CTA P receive slots (the S-CTA stages in 2)
-constexpr float kRescaleThreshold = 32.0f;    // log2 units: P <= 2^32
-constexpr float kMaxHeadroom = 64.0f;         // reference max set this far above a tile max
-constexpr float kMaxTileSum = 4294967296.0f;  // 2^kRescaleThreshold: bound on a half-tile sum
+// Budget of the lazy rescale (log2 units).  A row's reference max is set kHeadroom above
+// the tile max that moved it and moved again only when a tile's max exceeds it by more
+// than kThreshold, so P <= 2^kThreshold and O is rescaled only when the running max has
+// climbed by more than kThreshold + kHeadroom.  The narrow budget (32 / 64) keeps one
+// rescale factor 2^-d normal for every move whose dropped sums could still matter
+// (d <= 126 whenever they weigh more than 2^-30 of the new maximum).  The wide budget
+// (64 / 80) rescales less often on long contexts with outlying keys; it sends the factor
+// as a = 2^(-d/2) and every user multiplies by a twice, which stays normal up to d = 252,
+// beyond which the dropped sums weigh less than 2^-108 of the new maximum.
+template <bool kWide>
+struct Budget {
+  static constexpr float kThreshold = kWide ? 64.0f : 32.0f;
+  static constexpr float kHeadroom = kWide ? 80.0f : 64.0f;
+  static constexpr float kMaxTileSum = kWide ? 18446744073709551616.0f : 4294967296.0f;
+  // exponent of the factor that is sent: (m_old - m_new) / 2 for the wide budget
+  static constexpr float kFactorScale = kWide ? 0.5f : 1.0f;
+};
 constexpr int kThreads = 384;       // warps 0-3: roles; 4-11: softmax (S-CTA) / correction (O-CTA)
 constexpr uint32_t kColRope = 384;  // TMEM columns: Q latent 0..255, S 256..383, Q rope 384..415
 constexpr int kEvCorrect = 1;
@@ -111,7 +133,11 @@ enum Bar : int {
   // S-CTA: softmax warps <-> copy warp
   B_PSTAGED = 41,         // [2] P + sideband written into a staging slot (4 warps)
   B_STAGEFREE = 43,       // [2] the bulk copy has read the staging slot
-  B_COUNT = 45
+  // both CTAs: the MMA warp's last tcgen05 operations have completed (abort path)
+  B_DRAIN = 45,
+  // S-CTA: never arrived at; the copy warp waits on it when a test asks for a stall
+  B_NEVER = 46,
+  B_COUNT = 47
 };
 
 struct Params {
@@ -121,6 +147,11 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* gseq;
   int B, H, q_len, bs, num_blocks, max_blocks, cp, rank;
+  int causal;          // 0: every row of a block reads the shard's whole local sequence
+  int il;              // interleave: round-robin segments of il positions
+  long long span;      // cp * il
+  unsigned long long wait_ns;   // limit of every bounded wait
+  int stall_test;      // tests: the copy warp first waits for an arrival that never comes
   int shard_B;         // requests per shard (request b: q / gseq row b % shard_B, rank + b / shard_B)
   unsigned shard_mul;  // 0 for one shard, else ceil(2^32 / shard_B): b / shard_B = umulhi(b, shard_mul)
   int rows;            // H * q_len
@@ -154,12 +185,18 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t smem_base, int i) {
   return smem_base + kOffBar + 8 * i;
 }
 
-// Keys visible to row r (0-based within the request's q_len*H rows).
-__device__ __forceinline__ int row_bound(const Params& p, int r, long long G, int cap, int rank) {
+// Keys visible to row r (0-based within the request's q_len*H rows): the shard's share of
+// the row's global prefix under round-robin segments of il positions, at most cap.  Out of
+// line: it is needed once per segment, and its 64-bit divisions inlined at every call
+// site slowed the kernel's hot loops (code size; measured on GB300).
+__device__ __noinline__ int row_bound(const Params& p, int r, long long G, int cap, int rank) {
+  if (!p.causal) return cap;
   const int i = r / p.H;
   long long Gi = G - (p.q_len - 1 - i);
   if (Gi < 0) Gi = 0;
-  const long long loc = Gi / p.cp + ((Gi % p.cp) > rank ? 1 : 0);
+  long long rem = Gi % p.span - (long long)rank * p.il;
+  rem = rem < 0 ? 0 : (rem > p.il ? p.il : rem);
+  const long long loc = Gi / p.span * p.il + rem;
   return (int)(loc < cap ? loc : cap);
 }
 
@@ -343,7 +380,8 @@ __device__ __forceinline__ void set_abort_both(const SmemCtx& s, uint32_t peer) 
 // Bounded wait; on failure the abort word of both CTAs of the pair is set.
 __device__ __forceinline__ bool wait_bar(const SmemCtx& s, int i, uint32_t parity,
                                          const Params& p, bool cluster_scope = false) {
-  if (mbar_wait(bar_addr(s.base, i), parity, s.abort, p.status, cluster_scope)) return true;
+  if (mbar_wait(bar_addr(s.base, i), parity, s.abort, p.status, p.wait_ns, cluster_scope))
+    return true;
   set_abort_both(s, cluster_ctarank() ^ 1u);
   return false;
 }
@@ -416,6 +454,7 @@ __device__ __forceinline__ bool group_all(bool ok) {
   return r != 0;
 }
 
+template <bool kWide>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap,
@@ -471,6 +510,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(s.base, B_CORRDONE), 8);
     mbar_init(bar_addr(s.base, B_OFINAL), 1);
     mbar_init(bar_addr(s.base, B_OFREE), 8);
+    mbar_init(bar_addr(s.base, B_DRAIN), 1);
+    mbar_init(bar_addr(s.base, B_NEVER), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -670,6 +711,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++nseg;
         } while (seg_next(p, it));
       }
+      // every tcgen05 operation issued here completes before the CTA tears down (they read
+      // the key ring and write TMEM); after an abort nothing else has waited for them
+      mma_commit_warp(bar_addr(s.base, B_DRAIN));
+      mbar_wait_drain(bar_addr(s.base, B_DRAIN), 0);
     } else if (warp == 2) {
       // ---- copy warp: each staged P tile (+ sideband) into the O-CTA's receive slot -----
       // n % 3 once its previous tile there has been multiplied (the O-CTA's commit arrives
@@ -677,7 +722,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       SegIter it;
       long long n = 0;
       bool ok = true;
-      if (lane == 0 && seg_first(p, c, it, T, s_scan)) {
+      // a test of the timeout path: this wait runs out, and every role of the pair stops
+      if (p.stall_test && lane == 0) ok = wait_bar(s, B_NEVER, 0, p);
+      if (ok && lane == 0 && seg_first(p, c, it, T, s_scan)) {
         do {
           for (int t = it.t_begin; t < it.t_end && ok; ++t, ++n) {
             const int j = (int)(n & 1);
@@ -732,7 +779,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int t = it.t_begin; t < it.t_end; ++t, ++n) {
             const int g = (int)(n & 1);
             const int j = (int)(n & 1);            // P staging slot
-            if (!group_all(wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p))) {
+            // every exit from this loop is decided by all 256 threads together (they meet
+            // at named barriers), so a thread that failed a wait of its own leaves here
+            if (!group_all(!aborted && wait_bar(s, B_SFULL + g, (uint32_t)((n >> 1) & 1), p))) {
               aborted = true;
               break;
             }
@@ -772,9 +821,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               float t0, t1;
               f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), t0, t1);
               fsum = t0 + t1;
-              fast = fsum <= kMaxTileSum;
+              fast = fsum <= Budget<kWide>::kMaxTileSum;
             }
             const bool slow = bar_or_256(!fast);
+            using Bd = Budget<kWide>;
             if (!slow) {
               l += fsum;
             } else {
@@ -806,13 +856,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               asm volatile("bar.sync 1, 256;" ::: "memory");
               const float smax = fmaxf(hmax, xm[(hk ^ 1) * kM + r]);
               const float tmax = smax * p.scale_log2;
-              if (tmax > m_ref + kRescaleThreshold) {
-                const float m_new = tmax + kMaxHeadroom;
+              if (tmax > m_ref + Bd::kThreshold) {
+                const float m_new = tmax + Bd::kHeadroom;
                 if (m_ref != kNegInf) {
-                  alpha = fast_exp2(m_ref - m_new);
+                  alpha = fast_exp2((m_ref - m_new) * Bd::kFactorScale);
                   resc = true;
                 }
                 l *= alpha;
+                if (kWide) l *= alpha;
                 m_ref = m_new;
               }
               const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
@@ -859,10 +910,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const bool any_resc = __any_sync(0xffffffffu, resc);
 
-            // staging slot j must no longer be read by the copy of tile n-2
+            // staging slot j must no longer be read by the copy of tile n-2; a warp whose
+            // wait failed writes nothing and leaves at the next group-wide decision
             if (!warp_all(wait_bar(s, B_STAGEFREE + j, (uint32_t)(((n >> 1) & 1) ^ 1), p))) {
               aborted = true;
-              break;
+              continue;
             }
             uint8_t* slot = s.ptr + kOffP + j * kPSlotBytes;
             uint8_t* prow = slot + (r >> 3) * 1024 + (r & 7) * 128;
@@ -892,7 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (aborted || !group_all(*s.abort == 0)) break;
+          if (!group_all(!aborted && *s.abort == 0)) break;
           ++nseg;
         } while (seg_next(p, it));
       }
@@ -1044,6 +1096,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         warp_all(wait_bar(s, B_PVDONE, (uint32_t)(pv_phase & 1), p));
         ++pv_phase;
       }
+      mma_commit_warp(bar_addr(s.base, B_DRAIN));
+      mbar_wait_drain(bar_addr(s.base, B_DRAIN), 0);
     } else if (warp >= 4) {
       // ---- correction / epilogue warps: thread = row; warps w and w+4 share a TMEM lane
       // quadrant and take O's columns [256 hc, 256 hc + 256) ------------------------------
@@ -1078,7 +1132,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_off + c32 * 32, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
+                for (int k = 0; k < 32; ++k) {
+                  float x = __uint_as_float(v[k]) * a;
+                  if (kWide) x *= a;
+                  v[k] = __float_as_uint(x);
+                }
                 tmem_st32(tmem + lane_off + c32 * 32, v);
               }
               tmem_wait_st();
@@ -1170,7 +1228,11 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
     return;
   }
   if (p.whole_units) return;
-  const int2 m = p.meta[u];                   // first and last group holding the unit
+  int2 m = p.meta[u];                         // first and last group holding the unit
+  // kept inside [0, groups) whatever the workspace holds (a decode that gave up early
+  // may not have written it), so that every read below stays inside the workspace
+  m.x = min(max(m.x, 0), p.groups - 1);
+  m.y = min(max(m.y, m.x), p.groups - 1);
   if (m.x == m.y) return;                     // one cluster wrote the final result
   // groups between the first and the last owner hold a partial unless their tile range
   // is empty (possible when there are fewer tiles than groups); group cc's partial of
@@ -1239,16 +1301,20 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
     p.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * p.lse_mul : -INFINITY;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder() {
+  cudaDriverEntryPointQueryResult q;
+  void* f = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  return nullptr;
+}
+
+// Looked up once per process (a function-local static is initialised exactly once, also
+// when several host threads make their first call at the same time).
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encoder();
   return fn;
 }
 
@@ -1265,11 +1331,17 @@ int tc_clusters(int num_sms) { return num_sms / 2 > 0 ? num_sms / 2 : 1; }
 
 }  // namespace
 
+bool tc_block_size_ok(int bs) {
+  // a 64-key tile is 64 / bs whole pages (bs 16, 32) or part of one page (bs a multiple
+  // of 64); one TMA box never crosses a page
+  return bs == 16 || bs == 32 || (bs >= 64 && bs % 64 == 0);
+}
+
 bool tc_supported(const DecodeArgs& a) {
   const int bs = a.block_size;
   // every row tile of a request needs a cluster of its own (clusters = SMs / 2)
   if ((a.H * a.q_len + kM - 1) / kM > a.num_sms / 2) return false;
-  if (!(bs == 16 || bs == 32 || bs == 64 || bs == 128)) return false;
+  if (!tc_block_size_ok(bs)) return false;
   if ((long long)a.num_blocks * bs + 64 >= (1LL << 31)) return false;
   if (reinterpret_cast<uintptr_t>(a.kv) % 16 != 0) return false;
   return get_encoder() != nullptr;
@@ -1278,6 +1350,61 @@ bool tc_supported(const DecodeArgs& a) {
 size_t tc_workspace_size(int B, int H, int q_len, int num_sms) {
   const int rt = (H * q_len + kM - 1) / kM;
   return tc_ws_bytes(B * rt, tc_clusters(num_sms));
+}
+
+namespace {
+
+// Per-device set-up of the decode kernels, done once per device: the shared-memory
+// attribute of both budget instantiations and the number of clusters that can be
+// resident at once (the same for both: same block size and shared memory).
+struct TcDevice {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int active_clusters = 0;
+};
+constexpr int kMaxDevices = 64;
+TcDevice g_tc_dev[kMaxDevices];
+
+void tc_device_setup(TcDevice& d, int clusters_wanted) {
+  d.err = cudaFuncSetAttribute(mla_decode_tc_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (d.err == cudaSuccess)
+    d.err = cudaFuncSetAttribute(mla_decode_tc_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (d.err != cudaSuccess) return;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters_wanted);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, mla_decode_tc_kernel<false>, &cfg) == cudaSuccess &&
+      active > 0)
+    d.active_clusters = active;
+  cudaGetLastError();
+}
+
+}  // namespace
+
+namespace {
+std::atomic<int> g_budget_choice{0};   // 0 automatic, 1 narrow, 2 wide
+}
+
+void set_rescale_budget_choice(int choice) { g_budget_choice.store(choice); }
+
+bool tc_wide_budget(const DecodeArgs& a) {
+  const int choice = g_budget_choice.load();
+  if (choice != 0) return choice == 2;
+  // the running max climbs past the narrow budget mostly over long contexts (the largest
+  // of n scores keeps growing with n); the table spans max_blocks * block_size keys of
+  // each shard, cp_world times that globally
+  return (long long)a.max_blocks * a.block_size * a.cp_world >= (1LL << 18);
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
@@ -1302,6 +1429,11 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.max_blocks = a.max_blocks;
   p.cp = a.cp_world;
   p.rank = a.cp_rank;
+  p.causal = a.causal ? 1 : 0;
+  p.il = a.interleave;
+  p.span = (long long)a.cp_world * a.interleave;
+  p.wait_ns = a.wait_ns;
+  p.stall_test = a.stall_test;
   p.rows = a.H * a.q_len;
   p.row_tiles = (p.rows + kM - 1) / kM;
   p.units = a.B * p.row_tiles;
@@ -1314,40 +1446,14 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.status = a.status;
 
   int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_set[64] = {false};
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int C = tc_clusters(a.num_sms);
-  // the number of co-resident clusters depends only on the kernel and the device: asked
-  // once per device
-  static int active_clusters[64] = {0};
-  if (dev < 64 && active_clusters[dev] > 0) {
-    if (active_clusters[dev] < C) C = active_clusters[dev];
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * C);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, mla_decode_tc_kernel, &cfg) == cudaSuccess &&
-        active > 0) {
-      if (dev < 64) active_clusters[dev] = active;
-      if (active < C) C = active;
-    }
-    cudaGetLastError();
-  }
+  TcDevice& td = g_tc_dev[dev];
+  std::call_once(td.once, tc_device_setup, std::ref(td), C);
+  if (td.err != cudaSuccess) return td.err;
+  if (td.active_clusters > 0 && td.active_clusters < C) C = td.active_clusters;
   // whole groups of row_tiles clusters (row_tiles <= C is checked by tc_supported)
   p.groups = C / p.row_tiles;
   C = p.groups * p.row_tiles;
@@ -1416,8 +1522,11 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  mla_decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
-  cudaError_t e = cudaGetLastError();
+  if (tc_wide_budget(a))
+    mla_decode_tc_kernel<true><<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
+  else
+    mla_decode_tc_kernel<false><<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = (long long)p.units * kM;
   mla_tc_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);

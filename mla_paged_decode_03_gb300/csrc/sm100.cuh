@@ -2,9 +2,10 @@
 // mbarriers with bounded waits, TMA tile loads, bulk shared->cluster-shared copies,
 // cluster addressing, and the tcgen05 tensor-core / tensor-memory instructions.
 //
-// Every wait is bounded: it gives up after kWaitNs nanoseconds (or at once when the
-// CTA's abort word is set), sets MLA_STATUS_WAIT_TIMEOUT in the caller's status word and
-// returns false, so that a protocol error ends the kernel instead of hanging the GPU.
+// Every wait is bounded: it gives up after a limit in nanoseconds that the launch passes
+// (2 s unless a caller sets another; or at once when the CTA's abort word is set), sets
+// MLA_STATUS_WAIT_TIMEOUT in the caller's status word and returns false, so that a
+// protocol error ends the kernel instead of hanging the GPU.
 #pragma once
 
 #include <stdint.h>
@@ -14,7 +15,7 @@
 namespace mla {
 namespace sm100 {
 
-constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -88,17 +89,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return done != 0;
 }
 
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, unsigned int* status,
+                                                   unsigned long long limit_ns,
+                                                   bool cluster_scope);
+
 // Bounded wait for phase `parity` of `bar`.  `abort` is a CTA-shared word that any role
-// sets on failure so that every other role stops waiting at once.
+// sets on failure so that every other role stops waiting at once.  Only the first test is
+// inlined; the loop is out of line: inlined at every wait site of the decode kernel it
+// made the hot loops' code large enough to slow them by up to 60 % (measured on GB300).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status, bool cluster_scope = false) {
+                                          unsigned int* status, unsigned long long limit_ns,
+                                          bool cluster_scope = false) {
   if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, status, limit_ns, cluster_scope);
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, unsigned int* status,
+                                                   unsigned long long limit_ns,
+                                                   bool cluster_scope) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
       return true;
     if (*abort) return false;
-    if ((i & 63u) == 63u && globaltimer() - t0 > kWaitNs) {
+    if ((i & 63u) == 63u && globaltimer() - t0 > limit_ns) {
       *abort = 1;
       atomicOr(status, 8u);   // MLA_STATUS_WAIT_TIMEOUT
       return false;

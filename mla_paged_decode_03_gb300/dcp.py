@@ -2,13 +2,13 @@
 
 These prepare the inputs that a caller hands to ``mla_decode`` for one shard; they are
 not part of the timed decode step.  ``build_shard_pool`` places a request's KV rows into
-a shard's paged pool with the library's ``cp_local_slot`` kernel.
+a shard's paged pool with the library's ``cp_local_slot_scatter`` kernel.
 """
 from __future__ import annotations
 
 import torch
 
-from . import cp_local_slot
+from . import cp_local_slot_scatter
 
 __all__ = ["local_seq_lens", "build_shard_pool"]
 
@@ -28,22 +28,17 @@ def build_shard_pool(pool: torch.Tensor, kv_global: torch.Tensor, kv_offsets, G,
                      block_table: torch.Tensor, cp: int, rank: int,
                      interleave: int = 1) -> torch.Tensor:
     """Writes every global KV row this rank owns into ``pool`` [num_blocks, bs, 576] at
-    the slot ``cp_local_slot`` gives it.  kv_global [sum(G), 576] holds request b's rows
-    at kv_offsets[b]; block_table [B, max_blocks] int32 is shared by all shards."""
+    the slot ``cp_local_slot`` gives it, with the ``cp_local_slot_scatter`` kernel, one
+    request at a time.  kv_global [sum(G), 576] holds request b's rows at kv_offsets[b];
+    block_table [B, max_blocks] int32 is shared by all shards."""
     B = block_table.shape[0]
     G = [int(x) for x in G]
     offs = [int(x) for x in kv_offsets]
-    Gmax = max(G) if G else 0
-    if Gmax == 0:
-        return pool
     dev = pool.device
-    pos = torch.arange(Gmax, dtype=torch.int64, device=dev).repeat(B, 1)
-    lens = torch.tensor(G, dtype=torch.int64, device=dev).view(B, 1)
-    pos = torch.where(pos < lens, pos, torch.full_like(pos, -1))
-    slots = cp_local_slot(pos, block_table, pool.shape[1], cp, rank, interleave)
-    flat = pool.view(-1, pool.shape[2])
-    src_index = (torch.tensor(offs[:B], dtype=torch.int64, device=dev).view(B, 1)
-                 + torch.arange(Gmax, dtype=torch.int64, device=dev).view(1, Gmax))
-    own = slots >= 0
-    flat.index_copy_(0, slots[own], kv_global.index_select(0, src_index[own]))
+    for b in range(B):
+        if G[b] == 0:
+            continue
+        pos = torch.arange(G[b], dtype=torch.int64, device=dev).view(1, -1)
+        rows = kv_global[offs[b]:offs[b] + G[b]].view(1, G[b], -1)
+        cp_local_slot_scatter(pos, rows, block_table[b:b + 1], pool, cp, rank, interleave)
     return pool

@@ -18,7 +18,6 @@ import torch
 
 from . import _lib, alloc_workspace
 from . import _stream
-from .dcp import build_shard_pool, local_seq_lens
 
 
 def shard_major_block_table(block_table: torch.Tensor, pool_blocks: List[int]) -> torch.Tensor:
@@ -35,9 +34,17 @@ def shard_major_block_table(block_table: torch.Tensor, pool_blocks: List[int]) -
 
 
 class DcpDecodeStep:
+    """Buffers and calls of one layer step.  ``pools[r]`` / ``seq_lens[r]`` are shard r's
+    paged pool and local lengths, ``G`` the global lengths; ``causal`` False makes every
+    query row read its shard's whole sequence; ``interleave`` is the round-robin segment
+    length the pools were laid out with."""
+
     def __init__(self, q: torch.Tensor, block_table: torch.Tensor, G: torch.Tensor,
                  pools: List[torch.Tensor], seq_lens: List[torch.Tensor], q_len: int,
-                 scale: float, lse_base_e: bool, pool_all: Optional[torch.Tensor] = None):
+                 scale: float, lse_base_e: bool, pool_all: Optional[torch.Tensor] = None,
+                 causal: bool = True, interleave: int = 1):
+        self.causal = causal
+        self.interleave = interleave
         self.q = q
         self.block_table = block_table
         self.cp = len(pools)
@@ -62,26 +69,6 @@ class DcpDecodeStep:
                                                            [p.shape[0] for p in pools])
             self.seq_lens_all = torch.cat(seq_lens).contiguous()
         self.workspace = alloc_workspace(self.cp * B, H, q_len, dev)
-
-    @classmethod
-    def from_workload(cls, w, device: str = "cuda") -> "DcpDecodeStep":
-        """Builds the shard pools of a ``synth`` workload with the library's slot mapping
-        (unused slots stay NaN)."""
-        import synth  # input generator only: random draws, no method arithmetic
-
-        dev = torch.device(device)
-        q = w.q.to(dev)
-        kvg = w.kv_global.to(dev)
-        bt = w.block_table.to(dev)
-        pool_all = synth.poisoned_pool(w.cp * w.num_blocks, w.bs, dev)
-        pools, sls = [], []
-        for r in range(w.cp):
-            pool = pool_all[r * w.num_blocks:(r + 1) * w.num_blocks]
-            build_shard_pool(pool, kvg, w.kv_offsets, w.G.tolist(), bt, w.cp, r)
-            pools.append(pool)
-            sls.append(local_seq_lens(w.G, w.cp, r).to(dev))
-        del kvg
-        return cls(q, bt, w.G, pools, sls, w.q_len, w.scale, w.base_e, pool_all=pool_all)
 
     def kernel_launches_per_step(self) -> int:
         """Kernels one step launches: per shard the split-KV decode (+ its combine when
@@ -108,13 +95,15 @@ class DcpDecodeStep:
         wsb = ws.numel() * ws.element_size()
         base_e = 1 if self.lse_base_e else 0
         scale = float(self.scale)
+        causal = 1 if self.causal else 0
+        il = int(self.interleave)
         pool0 = self.pools[0]
         if self.cp == 1:
             _lib.check(L.mla_decode(
                 q.data_ptr(), pool0.data_ptr(), self.block_table.data_ptr(),
                 self.block_table.stride(0), self.seq_lens[0].data_ptr(), self.gseq.data_ptr(),
-                self.B, self.H, self.q_len, pool0.shape[1], pool0.shape[0],
-                self.block_table.shape[1], 1, 0, scale, self.out.data_ptr(),
+                self.B, self.H, self.q_len, causal, pool0.shape[1], pool0.shape[0],
+                self.block_table.shape[1], 1, 0, il, scale, self.out.data_ptr(),
                 self.out_lse.data_ptr(), base_e, ws.data_ptr(), wsb, st))
             return self.out, self.out_lse
         if self.batched:
@@ -122,8 +111,9 @@ class DcpDecodeStep:
             _lib.check(L.mla_decode_shards(
                 q.data_ptr(), self.pool_all.data_ptr(), bt.data_ptr(), bt.stride(0),
                 self.seq_lens_all.data_ptr(), self.gseq.data_ptr(), self.B, self.H, self.q_len,
-                pool0.shape[1], self.pool_all.shape[0], bt.shape[1], self.cp, scale,
-                self.partials.data_ptr(), self.lses.data_ptr(), base_e, ws.data_ptr(), wsb, st))
+                causal, pool0.shape[1], self.pool_all.shape[0], bt.shape[1], self.cp, il,
+                scale, self.partials.data_ptr(), self.lses.data_ptr(), base_e, ws.data_ptr(),
+                wsb, st))
         else:
             bt = self.block_table
             for r in range(self.cp):
@@ -131,8 +121,8 @@ class DcpDecodeStep:
                 _lib.check(L.mla_decode(
                     q.data_ptr(), pool.data_ptr(), bt.data_ptr(), bt.stride(0),
                     self.seq_lens[r].data_ptr(), self.gseq.data_ptr(), self.B, self.H,
-                    self.q_len, pool.shape[1], pool.shape[0], bt.shape[1], self.cp, r, scale,
-                    self.partials[r].data_ptr(), self.lses[r].data_ptr(), base_e,
+                    self.q_len, causal, pool.shape[1], pool.shape[0], bt.shape[1], self.cp, r,
+                    il, scale, self.partials[r].data_ptr(), self.lses[r].data_ptr(), base_e,
                     ws.data_ptr(), wsb, st))
         _lib.check(L.lse_merge(self.partials.data_ptr(), 0, self.lses.data_ptr(), self.cp,
                                self.T, self.H, self.out.data_ptr(), self.out_lse.data_ptr(),

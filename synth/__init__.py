@@ -74,6 +74,8 @@ class Workload:
     block_table: torch.Tensor    # int32 [B, max_blocks], shared by every shard's pool
     num_blocks: int              # pages in each shard's pool (the last one is a spare)
     slot_cases: List[SlotCase]
+    interleave: int = 1          # round-robin segment length of the KV sharding
+    causal: bool = True          # False: every query row sees the whole context
 
     @property
     def max_blocks(self) -> int:
@@ -99,9 +101,11 @@ def _randn_bf16(shape, gen, device):
 
 
 def make_workload(name: str, device: str = "cpu", lengths: Optional[List[int]] = None,
-                  B: Optional[int] = None) -> Workload:
+                  B: Optional[int] = None, draw_values: bool = True) -> Workload:
     """Draw one workload.  ``lengths``/``B`` shrink a workload for quick tests while
-    keeping its structure (head count, q_len, block size, shard count, LSE base)."""
+    keeping its structure (head count, q_len, block size, shard count, LSE base).  With
+    ``draw_values`` False the query and KV values are not drawn (empty tensors); the
+    lengths, block table and slot-mapping cases are the same as with them."""
     c = dict(CONFIGS[name])
     if B is not None:
         c["B"] = B
@@ -116,23 +120,29 @@ def make_workload(name: str, device: str = "cpu", lengths: Optional[List[int]] =
             c["B"] = len(G)
     Bn, H, q_len, bs, cp = c["B"], c["H"], c["q_len"], c["bs"], c["cp"]
 
-    dgen = torch.Generator(device=device).manual_seed(seed + 1000)
-    q = _randn_bf16((Bn, q_len, H, D_QK), dgen, device)
     total = int(G.sum())
-    kvf = torch.randn((total, D_QK), generator=dgen, dtype=torch.float32, device=device)
-    if c["outlier_frac"] > 0:
-        n_out = max(1, int(round(total * c["outlier_frac"])))
-        idx = torch.randint(0, total, (n_out,), generator=dgen, device=device)
-        kvf[idx] *= 20.0
-    kv_global = kvf.to(torch.bfloat16)
-    del kvf
+    if draw_values:
+        dgen = torch.Generator(device=device).manual_seed(seed + 1000)
+        q = _randn_bf16((Bn, q_len, H, D_QK), dgen, device)
+        kvf = torch.randn((total, D_QK), generator=dgen, dtype=torch.float32, device=device)
+        if c["outlier_frac"] > 0:
+            n_out = max(1, int(round(total * c["outlier_frac"])))
+            idx = torch.randint(0, total, (n_out,), generator=dgen, device=device)
+            kvf[idx] *= 20.0
+        kv_global = kvf.to(torch.bfloat16)
+        del kvf
+    else:
+        q = torch.empty((0,), dtype=torch.bfloat16, device=device)
+        kv_global = torch.empty((0, D_QK), dtype=torch.bfloat16, device=device)
     offsets = torch.zeros(Bn + 1, dtype=torch.int64)
     offsets[1:] = torch.cumsum(G, 0)
 
-    # Page budget per request and per shard: enough pages for ceil(G/cp) tokens,
-    # which bounds the share of any shard.  One spare column per row points at the
-    # spare page so that reads past a request's pages would be visible.
-    per_shard_tokens = (G + cp - 1) // cp
+    # Page budget per request and per shard: enough pages for ceil(G/span) segments of
+    # `interleave` tokens, which bounds the share of any shard.  One spare column per row
+    # points at the spare page so that reads past a request's pages would be visible.
+    il = int(c.get("interleave", 1))
+    span = cp * il
+    per_shard_tokens = (G + span - 1) // span * il
     pages = (per_shard_tokens + bs - 1) // bs
     total_pages = int(pages.sum())
     num_blocks = total_pages + 1
@@ -180,16 +190,20 @@ def make_workload(name: str, device: str = "cpu", lengths: Optional[List[int]] =
 
     return Workload(name=name, B=Bn, H=H, q_len=q_len, bs=bs, cp=cp, base_e=c["base_e"],
                     scale=SCALE, G=G, q=q, kv_global=kv_global, kv_offsets=offsets,
-                    block_table=bt, num_blocks=num_blocks, slot_cases=slot_cases)
+                    block_table=bt, num_blocks=num_blocks, slot_cases=slot_cases,
+                    interleave=il, causal=bool(c.get("causal", True)))
 
 
 def make_custom(B: int, H: int, q_len: int, lengths, bs: int, cp: int, base_e: bool = True,
                 seed: int = 0, outlier_frac: float = 0.0, device: str = "cpu",
-                spare_columns: int = 1) -> Workload:
-    """An ad-hoc workload with the same drawing rules (edge-case tests)."""
+                spare_columns: int = 1, interleave: int = 1, causal: bool = True) -> Workload:
+    """An ad-hoc workload with the same drawing rules (edge-case tests); ``interleave``
+    sizes the pages for round-robin segments of that length, ``causal`` False marks the
+    query blocks non-causal (every row sees the whole context)."""
     name = f"custom_{seed}"
     CONFIGS[name] = dict(B=B, H=H, q_len=q_len, ctx=tuple(lengths), bs=bs, cp=cp,
-                         base_e=base_e, seed=seed, outlier_frac=outlier_frac)
+                         base_e=base_e, seed=seed, outlier_frac=outlier_frac,
+                         interleave=interleave, causal=causal)
     try:
         w = make_workload(name, device=device, lengths=list(lengths))
     finally:

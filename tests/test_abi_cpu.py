@@ -49,18 +49,18 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.mla_abi_version() >> 16 == 1
+    assert lib.mla_abi_version() >> 16 == 2
 
 
 def _decode(lib, **kw):
-    a = dict(q=16, kv=16, bt=16, bt_stride=4, seq=16, gseq=16, B=1, H=16, q_len=1, bs=16,
-             num_blocks=4, max_blocks=4, cp=1, rank=0, scale=0.1, out=16, lse=16, base_e=1,
-             ws=None, ws_bytes=0)
+    a = dict(q=16, kv=16, bt=16, bt_stride=4, seq=16, gseq=16, B=1, H=16, q_len=1, causal=1,
+             bs=16, num_blocks=4, max_blocks=4, cp=1, rank=0, il=1, scale=0.1, out=16, lse=16,
+             base_e=1, ws=None, ws_bytes=0)
     a.update(kw)
     return lib.mla_decode(a["q"], a["kv"], a["bt"], a["bt_stride"], a["seq"], a["gseq"], a["B"],
-                          a["H"], a["q_len"], a["bs"], a["num_blocks"], a["max_blocks"], a["cp"],
-                          a["rank"], a["scale"], a["out"], a["lse"], a["base_e"], a["ws"],
-                          a["ws_bytes"], None)
+                          a["H"], a["q_len"], a["causal"], a["bs"], a["num_blocks"],
+                          a["max_blocks"], a["cp"], a["rank"], a["il"], a["scale"], a["out"],
+                          a["lse"], a["base_e"], a["ws"], a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -83,21 +83,31 @@ def _decode(lib, **kw):
     (dict(q=24), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(seq=18), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(ws=272, ws_bytes=1024), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(il=0), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(il=3), _lib.MLA_ERR_INVALID_ARGUMENT),          # must divide block_size 16
+    (dict(il=32), _lib.MLA_ERR_INVALID_ARGUMENT),
+    (dict(cp=2, gseq=None, causal=1), _lib.MLA_ERR_INVALID_ARGUMENT),
 ])
 def test_decode_rejects(lib, kw, code):
     assert _decode(lib, **kw) == code
     assert lib.mla_last_error().decode()
 
 
+def test_noncausal_decode_needs_no_global_lengths(lib):
+    # accepted by validation: without a GPU the call fails only where it needs the device
+    rc = _decode(lib, cp=2, rank=1, gseq=None, causal=0)
+    assert rc != _lib.MLA_ERR_INVALID_ARGUMENT, lib.mla_last_error()
+
+
 def _decode_shards(lib, **kw):
-    a = dict(q=16, kv=16, bt=16, bt_stride=4, seq=16, gseq=16, B=1, H=16, q_len=1, bs=16,
-             num_blocks=4, max_blocks=4, n=2, scale=0.1, out=16, lse=16, base_e=1,
+    a = dict(q=16, kv=16, bt=16, bt_stride=4, seq=16, gseq=16, B=1, H=16, q_len=1, causal=1,
+             bs=16, num_blocks=4, max_blocks=4, n=2, il=1, scale=0.1, out=16, lse=16, base_e=1,
              ws=None, ws_bytes=0)
     a.update(kw)
     return lib.mla_decode_shards(a["q"], a["kv"], a["bt"], a["bt_stride"], a["seq"], a["gseq"],
-                                 a["B"], a["H"], a["q_len"], a["bs"], a["num_blocks"],
-                                 a["max_blocks"], a["n"], a["scale"], a["out"], a["lse"],
-                                 a["base_e"], a["ws"], a["ws_bytes"], None)
+                                 a["B"], a["H"], a["q_len"], a["causal"], a["bs"],
+                                 a["num_blocks"], a["max_blocks"], a["n"], a["il"], a["scale"],
+                                 a["out"], a["lse"], a["base_e"], a["ws"], a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -112,6 +122,7 @@ def _decode_shards(lib, **kw):
     (dict(out=24), _lib.MLA_ERR_INVALID_ARGUMENT),
     (dict(B=1 << 20, H=1 << 8, q_len=16, n=16), _lib.MLA_ERR_UNSUPPORTED),  # rows past 2^31
     (dict(B=20000, n=16), _lib.MLA_ERR_UNSUPPORTED),     # n * B^2 >= 2^32
+    (dict(il=5), _lib.MLA_ERR_INVALID_ARGUMENT),
 ])
 def test_decode_shards_rejects(lib, kw, code):
     assert _decode_shards(lib, **kw) == code
@@ -146,6 +157,33 @@ def test_slot_rejects(lib):
     assert f(None, 16, 4, 4, 1, 8, 16, 2, 0, 1, 16, None) == E
     assert f(12, 16, 4, 4, 1, 8, 16, 2, 0, 1, 16, None) == E        # misaligned int64
     assert f(16, 16, 4, 4, 0, 8, 16, 2, 0, 1, 16, None) == _lib.MLA_OK
+    assert f(16, 16, 4, 4, 1 << 16, 1 << 16, 16, 2, 0, 1, 16, None) == _lib.MLA_ERR_UNSUPPORTED
+
+
+def test_scatter_rejects(lib):
+    E = _lib.MLA_ERR_INVALID_ARGUMENT
+    f = lib.cp_local_slot_scatter
+    # positions, kv_new, block_table, bt_stride, max_blocks, B, N, bs, cp, rank, il,
+    # kv_cache, num_blocks, slots, stream
+    ok = (16, 16, 16, 4, 4, 1, 8, 16, 2, 0, 1, 16, 4, None, None)
+
+    def call(**kw):
+        a = list(ok)
+        names = ["pos", "new", "bt", "stride", "maxb", "B", "N", "bs", "cp", "rank", "il", "kv",
+                 "nb", "slots", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(rank=2) == E
+    assert call(il=3) == E
+    assert call(nb=0) == E
+    assert call(new=None) == E
+    assert call(kv=None) == E
+    assert call(new=24) == E                                        # 8-byte aligned only
+    assert call(kv=40) == E
+    assert call(slots=12) == E
+    assert call(N=0) == _lib.MLA_OK
 
 
 def test_workspace_size_is_pure(lib):

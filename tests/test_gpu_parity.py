@@ -13,7 +13,7 @@ import mla_paged_decode_03_gb300 as M
 import oracle.mla_ref as R
 import synth
 from mla_paged_decode_03_gb300.dcp import build_shard_pool, local_seq_lens
-from mla_paged_decode_03_gb300.layer_step import DcpDecodeStep
+from step_builder import step_from_workload
 
 import gpu_helpers as H
 
@@ -61,33 +61,12 @@ def _slot_case_check(case):
 
 @pytest.mark.parametrize("name", ["tiny", "cp2", "long"])
 def test_cp_local_slot_workloads(name):
-    w = synth.make_workload(name)
+    # every position of every case, every rank, bit-exact (the long workload's case is
+    # 1,048,576 positions with cp_size 8: the oracle loops over them once per rank)
+    w = synth.make_workload(name, draw_values=False)
     assert w.slot_cases
     for case in w.slot_cases:
-        if case.positions.numel() > 300000:
-            # the oracle's per-position loop is slow: check a strided sample of rows'
-            # positions bit-exactly, and the whole output against the PAD pattern rules
-            _slot_large_check(case)
-        else:
-            _slot_case_check(case)
-
-
-def _slot_large_check(case):
-    pos, bt = case.positions, case.block_table
-    for rank in range(case.cp_size):
-        got = M.cp_local_slot(pos.to(DEV), bt.to(DEV), case.block_size, case.cp_size, rank,
-                              case.interleave).cpu().numpy()
-        idx = np.arange(0, pos.shape[1], 97)
-        want = R.ref_cp_local_slot(pos.numpy()[:, idx], bt.numpy(), case.block_size,
-                                   case.cp_size, rank, case.interleave)
-        assert np.array_equal(got[:, idx], want)
-        tail = slice(pos.shape[1] - 4096, pos.shape[1])
-        want_t = R.ref_cp_local_slot(pos.numpy()[:, tail], bt.numpy(), case.block_size,
-                                     case.cp_size, rank, case.interleave)
-        assert np.array_equal(got[:, tail], want_t)
-        owner = (pos.numpy() // case.interleave) % case.cp_size
-        assert np.array_equal(got >= 0, (owner == rank) & (pos.numpy() >= 0))
-    assert M.device_status() == 0
+        _slot_case_check(case)
 
 
 @pytest.mark.parametrize("bs,cp,il,N", [(16, 2, 1, 167), (64, 8, 1, 1000), (16, 4, 2, 333),
@@ -157,7 +136,7 @@ def test_lse_merge_skips_nan_partials_of_empty_shards():
 # mla_decode: whole workloads at sizes the oracle finishes in seconds
 # ---------------------------------------------------------------------------
 def _gpu_shards(w, with_workspace=True, batched=True):
-    step = DcpDecodeStep.from_workload(w, DEV)
+    step = step_from_workload(w, DEV)
     step.batched = batched and step.cp > 1
     if not with_workspace:
         step.workspace = torch.empty(0, dtype=torch.uint8, device=DEV)
@@ -268,7 +247,7 @@ def test_decode_without_workspace_matches(kernel):
 @pytest.mark.parametrize("q_len,lengths,cp", [
     (1, [1, 2, 3], 1), (2, [1, 2], 1), (3, [1, 2, 3, 4], 2), (4, [1, 3, 5, 9], 4),
     (4, [2, 17, 33], 16), (2, [15, 16, 17], 1), (3, [63, 64, 65, 127, 128, 129], 1),
-    (1, [191, 192, 193], 3), (8, [40, 300], 2),
+    (1, [191, 192, 193], 3), (8, [40, 300], 2), (16, [40, 300], 2), (16, [1, 17], 1),
 ])
 @pytest.mark.parametrize("H_,bs", [(16, 16), (64, 64), (128, 64)])
 def test_decode_edge_cases(q_len, lengths, cp, H_, bs, kernel):
@@ -352,7 +331,7 @@ def test_decode_seq_len_beyond_table_is_flagged(kernel):
 # ---------------------------------------------------------------------------
 def _sampled_full(name, sample, relative=False):
     w = synth.make_workload(name, device=DEV)
-    step = DcpDecodeStep.from_workload(w, DEV)
+    step = step_from_workload(w, DEV)
     out, lse = step.run()
     torch.cuda.synchronize()
     assert M.device_status() == 0
