@@ -393,6 +393,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 1/x and log2(x) on the SFU (rcp.approx / lg2.approx, relative error near 2^-23 and
+// absolute error near 2^-22): a row's 1/l and LSE, taken once per segment.
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Three-input maximum (a single instruction on this architecture).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -795,16 +808,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
             const int t0 = t * kTile;
             const int lim = lim_row - t0 - 32 * hk;   // valid keys of this row in the half
-            // Common case first: every key of both halves is valid and the running max
-            // already bounds this tile (no 2^x above 2^32, checked through the sum).  All 256
-            // threads then keep the running max, and one barrier with an OR-reduction tells
-            // them whether any row needs the full step below (a new max, a partial half, or
-            // a unit's first tile), which all of them then take.
+            // keys of the half this row does not see score -inf: weight exactly 0, whatever
+            // their cache slot holds, so one code path serves whole and partial halves
+            if (lim < 32) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (k >= lim) sv[k] = 0xff800000u;
+            }
+            // Common case first: the running max already bounds this tile (no 2^x above
+            // 2^threshold, checked through the sum).  All 256 threads then keep the running
+            // max, and one barrier with an OR-reduction tells them whether any row needs the
+            // full step below (a new max, or a unit's first tile), which all of them then
+            // take.
             float alpha = 1.f;
             bool resc = false;
             uint32_t pk[16];
             float fsum = 0.f;
-            bool fast = (lim >= 32) && (m_ref != kNegInf);
+            bool fast = m_ref != kNegInf;
             if (fast) {
               const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
               const uint64_t nm2 = f32x2(-m_ref, -m_ref);
@@ -828,29 +848,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!slow) {
               l += fsum;
             } else {
-              // running max on the raw scores (scale > 0 keeps the order), in log2 units.  A
-              // whole half (the common case) takes three-input maxima and paired fp32
-              // arithmetic, so that these warps leave issue slots to the MMA warp that shares
-              // their scheduler; a partial half masks key by key.
-              float hmax;
-              if (lim >= 32) {
-                float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+              // running max on the raw scores (scale > 0 keeps the order), in log2 units,
+              // with three-input maxima and paired fp32 arithmetic, so that these warps leave
+              // issue slots to the MMA warp that shares their scheduler
+              float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-                for (int k = 0; k < 32; k += 8)
+              for (int k = 0; k < 32; k += 8)
 #pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    m4[q] = fmax3(m4[q], __uint_as_float(sv[k + 2 * q]), __uint_as_float(sv[k + 2 * q + 1]));
-                hmax = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-              } else {
-                float mx8[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mx8[q] = kNegInf;
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                  if (k < lim) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[k]));
-                hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-              }
+                for (int q = 0; q < 4; ++q)
+                  m4[q] = fmax3(m4[q], __uint_as_float(sv[k + 2 * q]), __uint_as_float(sv[k + 2 * q + 1]));
+              const float hmax = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
               float* xm = xmax + (n & 1) * 2 * kM;
               xm[hk * kM + r] = hmax;
               asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -867,39 +874,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
               }
               const float neg_mu = (m_ref == kNegInf) ? 0.f : -m_ref;
-              if (lim >= 32) {
-                // e = 2^(s * scale_log2 - m) two keys per instruction (each lane rounds as fmaf)
-                const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
-                const uint64_t nm2 = f32x2(neg_mu, neg_mu);
-                uint64_t s2[4] = {0, 0, 0, 0};
+              // e = 2^(s * scale_log2 - m) two keys per instruction (each lane rounds as fmaf)
+              const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+              const uint64_t nm2 = f32x2(neg_mu, neg_mu);
+              uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  float y0, y1;
-                  f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
-                                        sc2, nm2), y0, y1);
-                  const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
-                  s2[k & 3] = add_f32x2(s2[k & 3], f32x2(e0, e1));
-                  pk[k] = pack_bf16x2(e0, e1);
-                }
-                float t0, t1;
-                f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), t0, t1);
-                l += t0 + t1;
-              } else {
-                float sum8[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const float e0 = 2 * k < lim
-                      ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), p.scale_log2, neg_mu)) : 0.f;
-                  const float e1 = 2 * k + 1 < lim
-                      ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), p.scale_log2, neg_mu)) : 0.f;
-                  sum8[k & 7] += e0 + e1;
-                  pk[k] = pack_bf16x2(e0, e1);
-                }
-                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                     ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+              for (int k = 0; k < 16; ++k) {
+                float y0, y1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
+                                      sc2, nm2), y0, y1);
+                const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+                s2[k & 3] = add_f32x2(s2[k & 3], f32x2(e0, e1));
+                pk[k] = pack_bf16x2(e0, e1);
               }
+              float t0, t1;
+              f32x2_split(add_f32x2(add_f32x2(s2[0], s2[1]), add_f32x2(s2[2], s2[3])), t0, t1);
+              l += t0 + t1;
             }
             const bool last = (t + 1 == it.t_end);
             float l_row = 0.f;                     // the whole row's sum, on the last tile
@@ -927,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               // the O-CTA reads the factors only after a step that may rescale (taken by all
               // rows together), and 1 / l only on a unit's last tile
               if (slow) side[r] = alpha;
-              if (last) side[128 + r] = l_row > 0.f ? 1.f / l_row : 0.f;
+              if (last) side[128 + r] = l_row > 0.f ? fast_rcp(l_row) : 0.f;
               int* flags = reinterpret_cast<int*>(slot + kPBytes + 1024);
               if (lane == 0) flags[q4] = any_resc ? 1 : 0;
             }
@@ -935,7 +925,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(s.base, B_PSTAGED + j));
             if (last && valid && hk == 0) {
-              const float lse2 = l_row > 0.f ? m_ref + log2f(l_row) : kNegInf;
+              const float lse2 = l_row > 0.f ? m_ref + fast_log2(l_row) : kNegInf;
               const long long grow = (long long)b * p.rows + row;
               if (it.single) {
                 if (p.lse != nullptr) p.lse[grow] = lse2 * p.lse_mul;
