@@ -268,6 +268,48 @@ def time_slot(steps, warmup, device, flush):
                 calls=len(times))
 
 
+def time_scatter(steps, warmup, device, flush):
+    """cp_local_slot_scatter over the same 1,048,576 positions (cp_size 8), one call per
+    rank, each writing the 576-dim bf16 rows of the positions it owns into its pool.
+    HBM-bound: 8 B of position per position, plus 2 x 1152 B (row read and written) per
+    owned position."""
+    import mla_paged_decode_03_gb300 as m
+
+    case = synth.make_workload("long", draw_values=False).slot_cases[0]
+    pos = case.positions.to(device)
+    bt = case.block_table.to(device)
+    B, N = pos.shape
+    g = torch.Generator(device=device).manual_seed(7)
+    kv_new = torch.randn(B, N, 576, generator=g, device=device).to(torch.bfloat16)
+    num_blocks = int(bt.max()) + 1
+    pool = torch.empty(num_blocks, case.block_size, 576, dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        m.cp_local_slot_scatter(pos, kv_new, bt, pool, case.cp_size, 0, case.interleave)
+    torch.cuda.synchronize()
+    times, owned = [], []
+    for k in range(steps):
+        for rank in range(case.cp_size):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            m.cp_local_slot_scatter(pos, kv_new, bt, pool, case.cp_size, rank, case.interleave)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+            if k == 0:
+                owned.append(int((((pos >= 0) & ((pos // case.interleave) % case.cp_size == rank))
+                                  .sum()).item()))
+    assert m.device_status() == 0
+    n = pos.numel()
+    us = statistics.mean(times) * 1e3
+    nbytes = 8.0 * n + 2304.0 * statistics.mean(owned)
+    return dict(us_per_call=us, positions=n, cp_size=case.cp_size,
+                owned_per_call=statistics.mean(owned), bytes_per_call=nbytes,
+                gbs=nbytes / (us * 1e-6) / 1e9, calls=len(times))
+
+
 def time_e2e(step, steps, warmup, flush):
     """Same step through the public API with host buffers: every step copies the
     per-step inputs (q, block table, lengths) from pinned host memory and reads the
@@ -424,10 +466,13 @@ def run_ours(args):
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
+    if args.decode_kernel == "mma":
+        m.set_decode_kernel(m.KERNEL_MMA)
     if args.slot_only:
         r = time_slot(max(1, args.steps), args.warmup, device, flush)
+        r2 = time_scatter(max(1, args.steps), args.warmup, device, flush)
         if rank == 0:
-            print(json.dumps({"cp_local_slot_1M": r}))
+            print(json.dumps({"cp_local_slot_1M": r, "cp_local_slot_scatter_1M": r2}))
         return
 
     per_config = {}
@@ -442,6 +487,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
     if args.extra_configs:
         per_config["cp_local_slot_1M"] = time_slot(max(3, args.steps) // 3 + 1, 3, device, flush)
+        per_config["cp_local_slot_scatter_1M"] = time_scatter(max(3, args.steps) // 3 + 1, 3,
+                                                              device, flush)
+        torch.cuda.empty_cache()
 
     if ws > 1:
         import torch.distributed as dist
@@ -547,7 +595,10 @@ def main():
     ap.add_argument("--config", default="spec", choices=synth.ORDER)
     ap.add_argument("--extra-configs", default="tiny,cp2,plain,long")
     ap.add_argument("--slot-only", action="store_true",
-                    help="time only cp_local_slot on the 1,048,576-position case")
+                    help="time only cp_local_slot and cp_local_slot_scatter on the "
+                         "1,048,576-position case")
+    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "mma"],
+                    help="profiling only: run the warp-level cross-check decode kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the headline workload's batch (profiling runs only)")

@@ -16,8 +16,8 @@
 // kernel issue-bound (about 170 instructions per position).
 //
 // The scatter additionally copies each owned position's 1152-byte row (576 bf16) from
-// the new rows to its slot, one warp per position (512 contiguous bytes per warp
-// instruction); positions this rank does not own are neither read nor written.
+// the new rows to its slot (512 contiguous bytes per warp instruction); positions this rank
+// does not own are neither read nor written.
 #include "internal.h"
 #include "../../include/mla_decode.h"
 
@@ -106,31 +106,65 @@ __global__ void __launch_bounds__(256) cp_local_slot_scalar(const long long* __r
   if (bad) atomicOr(p.status, MLA_STATUS_BAD_VBLOCK);
 }
 
-// One warp per position: map it, and copy its row when this rank owns it and the page is
-// inside the cache.  `slots` (may be null) receives the mapping, as cp_local_slot gives it.
+// A warp takes 32 consecutive positions: each lane maps one (coalesced position loads and
+// slot stores), then the warp copies the rows of the owned ones, four rows per round so that
+// every lane has several 16-byte loads in flight before it stores.  `slots` (may be null)
+// receives the mapping, as cp_local_slot gives it.
 __global__ void __launch_bounds__(256) cp_local_slot_scatter_kernel(
     const long long* __restrict__ pos, const uint4* __restrict__ kv_new,
     uint4* __restrict__ kv_cache, long long* __restrict__ slots, long long total,
     long long cache_rows, FastDiv div_row, SlotParams p) {
   const int lane = threadIdx.x & 31;
   bool bad_vb = false, bad_page = false;
-  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; i < total;
-       i += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int b = (int)fdiv((unsigned int)i, div_row);
-    const long long slot = map_one(__ldg(pos + i), b, p, bad_vb);
-    if (slots != nullptr && lane == 0) slots[i] = slot;
-    if (slot < 0) continue;
-    if (slot >= cache_rows) {
-      bad_page = true;
-      continue;
+  const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long g = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; g * 32 < total;
+       g += warps) {
+    const long long i = g * 32 + lane;
+    long long slot = MLA_PAD_SLOT_ID;
+    if (i < total) {
+      slot = map_one(__ldg(pos + i), (int)fdiv((unsigned int)i, div_row), p, bad_vb);
+      if (slots != nullptr) slots[i] = slot;
+      if (slot >= cache_rows) {
+        bad_page = true;
+        slot = MLA_PAD_SLOT_ID;
+      }
     }
-    const uint4* src = kv_new + i * kRowChunks;
-    uint4* dst = kv_cache + slot * kRowChunks;
+    unsigned int own = __ballot_sync(0xffffffffu, slot >= 0);
+    while (own != 0u) {
+      int src[4];
+      long long dst[4];
+      int nr = 0;
 #pragma unroll
-    for (int c = lane; c < kRowChunks; c += 32) __stcs(dst + c, __ldcs(src + c));
+      for (int u = 0; u < 4; ++u) {
+        src[u] = 0;
+        dst[u] = -1;
+        if (own != 0u) {
+          const int l = __ffs(own) - 1;
+          own &= own - 1u;
+          src[u] = l;
+          dst[u] = __shfl_sync(0xffffffffu, slot, l);
+          nr = u + 1;
+        }
+      }
+      uint4 v[4][3];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const int ch = lane + 32 * c;
+          if (u < nr && ch < kRowChunks) v[u][c] = __ldcs(kv_new + (g * 32 + src[u]) * kRowChunks + ch);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const int ch = lane + 32 * c;
+          if (u < nr && ch < kRowChunks) __stcs(kv_cache + dst[u] * kRowChunks + ch, v[u][c]);
+        }
+    }
   }
-  if (lane == 0 && bad_vb) atomicOr(p.status, MLA_STATUS_BAD_VBLOCK);
-  if (lane == 0 && bad_page) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+  if (__any_sync(0xffffffffu, bad_vb) && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_VBLOCK);
+  if (__any_sync(0xffffffffu, bad_page) && lane == 0) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
 }
 
 SlotParams make_params(const int32_t* block_table, int64_t bt_stride, int max_blocks,
@@ -204,7 +238,7 @@ cudaError_t launch_cp_local_slot_scatter(const int64_t* positions, const uint16_
   const SlotParams p = make_params(block_table, bt_stride, max_blocks, block_size, cp_size,
                                    cp_rank, interleave, status);
   const int sms = sm_count();
-  long long blocks = (total + 7) / 8;            // 8 warps per block, one per position
+  long long blocks = (total + 255) / 256;        // 8 warps per block, 32 positions per warp
   const long long cap = (long long)sms * 16;
   if (blocks > cap) blocks = cap;
   cp_local_slot_scatter_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
