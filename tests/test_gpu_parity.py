@@ -251,9 +251,12 @@ def test_decode_without_workspace_matches(kernel):
 ])
 @pytest.mark.parametrize("H_,bs", [(16, 16), (64, 64), (128, 64)])
 def test_decode_edge_cases(q_len, lengths, cp, H_, bs, kernel):
+    # a few keys per shard (down to one): outputs come close to a single |V|, where the
+    # bf16 roundings of P, of a split partial and of the output approach 2e-2, so these
+    # cases use the derived per-element bound of gpu_helpers (never below 2e-2)
     w = synth.make_custom(len(lengths), H_, q_len, lengths, bs, cp, base_e=(cp != 4),
                           seed=q_len * 100 + cp + H_)
-    _check_workload(w)
+    _check_workload(w, relative=True)
 
 
 def _offset_16(t):
