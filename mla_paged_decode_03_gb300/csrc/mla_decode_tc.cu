@@ -1197,19 +1197,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge the partials of units that were cut between clusters; units with no visible key
-// get out = 0 and lse = -inf.  One warp per (unit, row).
-__global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
-  const int lane = threadIdx.x & 31;
-  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wid >= (long long)p.units * kM) return;
-  const int u = (int)(wid / kM), r = (int)(wid % kM);
-  const int b = u / p.row_tiles, rt = u % p.row_tiles;
+// get out = 0 and lse = -inf.  A warp per (unit, row); the first thread of each block of
+// 8 rows decides once for the block whether the unit needs anything (most units were
+// finished by one cluster), instead of every warp working out the unit's tile count.
+__device__ __forceinline__ void combine_row(const Params& p, int b, int rt, int r,
+                                            int lane, int nt, int2 m) {
   const int row = rt * kM + r;
-  if (row >= p.rows) return;
   const long long grow = (long long)b * p.rows + row;
-  if (rt == 0 && r == 0 && lane == 0 && __ldg(p.seq_lens + b) > p.max_blocks * p.bs)
-    atomicOr(p.status, MLA_STATUS_SEQ_TOO_LONG);
-  const int nt = unit_tiles(p, u);
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kDv;
   if (nt == 0) {
     *reinterpret_cast<uint4*>(o + 8 * lane) = make_uint4(0, 0, 0, 0);
@@ -1217,16 +1211,6 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
     if (p.lse != nullptr && lane == 0) p.lse[grow] = -INFINITY;
     return;
   }
-  if (p.whole_units) return;
-  int2 m = p.meta[u];                         // first and last group holding the unit
-  // kept inside [0, groups) whatever the workspace holds (a decode that gave up early
-  // may not have written it), so that every read below stays inside the workspace
-  m.x = min(max(m.x, 0), p.groups - 1);
-  m.y = min(max(m.y, m.x), p.groups - 1);
-  if (m.x == m.y) return;                     // one cluster wrote the final result
-  // groups between the first and the last owner hold a partial unless their tile range
-  // is empty (possible when there are fewer tiles than groups); group cc's partial of
-  // unit u is in slot (b + cc) * R + rt
   const long long T = p.hdr[0];
   auto holds = [&](int cc) {
     return range_start(T, cc, p.groups) < range_start(T, cc + 1, p.groups);
@@ -1289,6 +1273,36 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   }
   if (p.lse != nullptr && lane == 0)
     p.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * p.lse_mul : -INFINITY;
+}
+
+__global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
+  __shared__ int s_nt;
+  __shared__ int2 s_m;
+  const int u = blockIdx.x >> 4, rb = blockIdx.x & 15;      // 16 blocks of 8 rows per unit
+  const int b = u / p.row_tiles, rt = u % p.row_tiles;
+  if (threadIdx.x == 0) {
+    if (rt == 0 && rb == 0 && __ldg(p.seq_lens + b) > p.max_blocks * p.bs)
+      atomicOr(p.status, MLA_STATUS_SEQ_TOO_LONG);
+    const int nt = unit_tiles(p, u);
+    int2 m = make_int2(0, 0);
+    if (nt > 0 && !p.whole_units) {
+      m = p.meta[u];                          // first and last group holding the unit
+      // kept inside [0, groups) whatever the workspace holds (a decode that gave up early
+      // may not have written it), so that every read stays inside the workspace
+      m.x = min(max(m.x, 0), p.groups - 1);
+      m.y = min(max(m.y, m.x), p.groups - 1);
+    }
+    s_nt = nt;
+    s_m = m;
+  }
+  __syncthreads();
+  const int nt = s_nt;
+  const int2 m = s_m;
+  // one cluster wrote the final result (or there is no workspace): nothing to do
+  if (nt > 0 && (p.whole_units || m.x == m.y)) return;
+  const int r = rb * 8 + (threadIdx.x >> 5);
+  if (rt * kM + r >= p.rows) return;
+  combine_row(p, b, rt, r, threadIdx.x & 31, nt, m);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder() {
@@ -1518,8 +1532,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     mla_decode_tc_kernel<false><<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long warps = (long long)p.units * kM;
-  mla_tc_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+  mla_tc_combine_kernel<<<(unsigned)p.units * 16u, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

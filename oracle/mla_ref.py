@@ -14,7 +14,7 @@ Sources (web pages summarising three vLLM pull requests):
   [#54012] "带 DCP 的 MLA decode 改用 FlashInfer 原生 CP mask" (vLLM PR 54012)
   [#48180] "为 TokenSpeed MLA 后端添加 DCP 与 Eagle 支持" (vLLM PR 48180)
 
-Readings of points the pages leave open (each also listed in the design notes):
+Readings of points the pages leave open:
   * PAD_SLOT_ID is -1; a negative position means "rejected" and maps to PAD.
   * Query/KV head dim 576 = 512 latent + 64 rope; V is the first 512 dims of each row.
   * A query row with no visible key gets out = 0 and lse = -inf; a merge gives such a
