@@ -152,6 +152,7 @@ struct Params {
   long long span;      // cp * il
   unsigned long long wait_ns;   // limit of every bounded wait
   int stall_test;      // tests: the copy warp first waits for an arrival that never comes
+  int seg_tiles;       // start-up share of a request on the split line, in tiles
   int shard_B;         // requests per shard (request b: q / gseq row b % shard_B, rank + b / shard_B)
   unsigned shard_mul;  // 0 for one shard, else ceil(2^32 / shard_B): b / shard_B = umulhi(b, shard_mul)
   int rows;            // H * q_len
@@ -167,7 +168,7 @@ struct Params {
   float lse_mul;
   uint16_t* out;
   float* lse;
-  long long* hdr;      // workspace header: [0] = total tiles T of this call
+  long long* hdr;      // workspace header: [0] = length T of this call's split line
   int2* meta;          // [units] first / last cluster of each unit
   float* ws_lse;       // [units + C][128]
   uint16_t* ws_o;      // [units + C][128][512] normalised partial outputs, bf16
@@ -230,13 +231,22 @@ __device__ __forceinline__ int req_tiles(const Params& p, int b) {
   return unit_tiles(p, b * p.row_tiles + p.row_tiles - 1);
 }
 
-// Work split.  The clusters form G groups of R = row_tiles clusters; group g takes the
-// request tiles [g*T/G, (g+1)*T/G) of the concatenation of all requests' tiles, and its
-// cluster g*R + rt runs row tile rt of those tiles, so that the R units of a request read
-// the same keys at the same time (from L2 after the first).  A unit's range is clamped to
-// its own tile count (at most one fewer than its request's).  SegIter walks the segments
-// (unit, tile range) of one cluster in order; every role of both CTAs of the pair runs its
-// own copy of it and sees the same sequence.
+// Length of request b on the split line: its tiles plus the start-up share p.seg_tiles
+// (none when it has no tile).
+__device__ __forceinline__ long long req_span(const Params& p, int b) {
+  const int nt = req_tiles(p, b);
+  return nt > 0 ? (long long)nt + p.seg_tiles : 0;
+}
+
+// Work split.  The clusters form G groups of R = row_tiles clusters.  The requests' tiles
+// are laid end to end, each request with a tile preceded by seg_tiles positions that stand
+// for the cost of starting a segment; group g takes the positions [g*T/G, (g+1)*T/G) of
+// that line (T = its length), and its cluster g*R + rt runs row tile rt of the tiles among
+// them, so that the R units of a request read the same keys at the same time (from L2
+// after the first).  A unit's range is clamped to its own tile count (at most one fewer
+// than its request's).  SegIter walks the segments (unit, tile range) of one cluster in
+// order; every role of both CTAs of the pair runs its own copy of it and sees the same
+// sequence.
 struct SegIter {
   int u;            // current unit = b * row_tiles + rt
   int b;            // its request
@@ -244,7 +254,7 @@ struct SegIter {
   int grp;          // this cluster's group
   int t_begin;      // first tile of the segment within the unit
   int t_end;        // one past the last tile
-  long long g0;     // index of request b's first tile in the concatenation
+  long long g0;     // position of request b's first tile on the split line
   long long g_end;  // end of the group's range
   bool whole;
   bool single;      // the segment covers the whole unit
@@ -286,7 +296,8 @@ __device__ bool seg_next(const Params& p, SegIter& it) {
     return false;
   }
   for (;;) {
-    const long long g = it.g0 + req_tiles(p, it.b);   // next request's first tile
+    // the next request's first tile, after its start-up share
+    const long long g = it.g0 + req_tiles(p, it.b) + p.seg_tiles;
     if (g >= it.g_end) return false;
     int b = it.b + 1;
     while (b < p.B && req_tiles(p, b) == 0) ++b;
@@ -297,8 +308,9 @@ __device__ bool seg_next(const Params& p, SegIter& it) {
   }
 }
 
-// First segment of cluster c, or none.  s_scan holds the request containing the group's
-// first tile and that request's first tile index (from the prologue's scan).
+// First segment of cluster c, or none.  s_scan holds the request whose span contains the
+// group's first position and that request's first tile position (from the prologue's
+// scan); a range that starts inside a start-up share starts at the request's first tile.
 __device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int* s_scan) {
   it.grp = c / p.row_tiles;
   it.rt = c % p.row_tiles;
@@ -318,7 +330,7 @@ __device__ bool seg_first(const Params& p, int c, SegIter& it, long long T, int*
   it.b = s_scan[0];
   it.g0 = ((long long)s_scan[2] << 32) | (unsigned)s_scan[1];
   it.g_end = e;
-  return seg_set(p, it, (int)(a - it.g0)) || seg_next(p, it);
+  return seg_set(p, it, a > it.g0 ? (int)(a - it.g0) : 0) || seg_next(p, it);
 }
 
 // Cache rows of a segment's TMA boxes for a producer warp: box i covers box_rows keys
@@ -532,49 +544,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
 
-  // schedule: total request tiles T and the request holding this group's first tile
+  // schedule: the length T of the split line and the request holding this group's first
+  // position
   long long T = 0;
   {
-    __shared__ long long s_total;
-    __shared__ int s_warp[kThreads / 32];
-    const long long a_start_guess = -1;
-    (void)a_start_guess;
-    if (tid == 0) {
-      s_total = 0;
-      s_scan[0] = -1;
-    }
-    __syncthreads();
-    // pass 1: T
+    __shared__ long long s_warp[kThreads / 32];
+    if (tid == 0) s_scan[0] = -1;
+    // pass 1: T, summed per warp (one shared 64-bit atomic per thread made this pass
+    // ~10 us longer at 256 requests, measured on GB300)
     long long local = 0;
-    for (int b = tid; b < p.B; b += kThreads) local += req_tiles(p, b);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)local);
+    for (int b = tid; b < p.B; b += kThreads) local += req_span(p, b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0) s_warp[warp] = local;
     __syncthreads();
-    T = s_total;
+    for (int w = 0; w < kThreads / 32; ++w) T += s_warp[w];
+    __syncthreads();
     if (!p.whole_units && T > 0 && c / p.row_tiles < p.groups) {
       const long long a = range_start(T, c / p.row_tiles, p.groups);
-      // pass 2: chunked exclusive scan to find the request containing tile a
+      // pass 2: chunked exclusive scan to find the request whose span contains position a
       long long running = 0;
       for (int base = 0; base < p.B; base += kThreads) {
         const int u = base + tid;          // a request index here
-        const int nt = u < p.B ? req_tiles(p, u) : 0;
-        int incl = nt;
+        const long long nt = u < p.B ? req_span(p, u) : 0;
+        long long incl = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          const long long v = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += v;
         }
         if (lane == 31) s_warp[warp] = incl;
         __syncthreads();
-        int wpre = 0, total = 0;
+        long long wpre = 0, total = 0;
         for (int w = 0; w < kThreads / 32; ++w) {
           if (w < warp) wpre += s_warp[w];
           total += s_warp[w];
         }
         const long long excl = running + wpre + incl - nt;
         if (u < p.B && nt > 0 && excl <= a && a < excl + nt) {
+          const long long first = excl + p.seg_tiles;   // the request's first tile position
           s_scan[0] = u;
-          s_scan[1] = (int)(excl & 0xffffffffLL);
-          s_scan[2] = (int)(excl >> 32);
+          s_scan[1] = (int)(first & 0xffffffffLL);
+          s_scan[2] = (int)(first >> 32);
         }
         running += total;
         __syncthreads();
@@ -1462,6 +1473,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   p.groups = C / p.row_tiles;
   C = p.groups * p.row_tiles;
   p.clusters = C;
+  // starting a segment (the output tile drained and written, the next unit's Q loaded, the
+  // key ring refilled) takes about as long as 6 tiles: 4-7 us against ~1 us a tile (GB300)
+  p.seg_tiles = 6;
   const size_t need = tc_ws_bytes(p.units, C);
   if (a.workspace != nullptr && a.workspace_bytes >= need) {
     char* ws = static_cast<char*>(a.workspace);
