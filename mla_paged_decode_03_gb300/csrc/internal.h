@@ -88,6 +88,26 @@ cudaError_t launch_lse_combine(const void* partials, bool partials_fp32, const f
 // Fast division of 32-bit numerators by a fixed divisor d >= 1: q = mulhi64(m, n) with
 // m = floor((2^64 - 1) / d) + 1 is exact for every n < 2^32 (Lemire, Kaser and Kurz,
 // "Faster remainder by direct computation", 2019); d = 1 is kept apart (m would be 2^64).
+// Launch configuration of a kernel that consumes the previous kernel's results in the same
+// stream (programmatic dependent launch): the kernel may be scheduled while that kernel
+// drains, and waits for its completion and memory with griddepcontrol.wait before it reads
+// or writes global memory.  Without the attribute (or after a non-kernel operation) the
+// wait returns at once.
+struct DependentLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  DependentLaunch(dim3 grid, dim3 block, cudaStream_t stream) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
 struct FastDiv {
   unsigned long long m;
   unsigned int d;

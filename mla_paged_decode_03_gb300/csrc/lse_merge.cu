@@ -45,6 +45,8 @@ lse_combine_kernel(const T* __restrict__ partials, const float* __restrict__ lse
                    long long rows, long long shard_stride_rows, float lse_to_log2,
                    float out_lse_mul, __nv_bfloat16* __restrict__ out,
                    float* __restrict__ out_lse) {
+  // launched as a dependent of the kernel that wrote the partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -99,16 +101,15 @@ cudaError_t launch_lse_combine(const void* partials, bool partials_fp32, const f
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows + kWarps - 1) / kWarps;
   const float k = in_log2 ? 1.0f : 1.4426950408889634f;
-  if (partials_fp32) {
-    lse_combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
-        static_cast<const float*>(partials), lses, n, rows, shard_stride_rows, k, out_lse_mul,
-        reinterpret_cast<__nv_bfloat16*>(out), out_lse);
-  } else {
-    lse_combine_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(partials), lses, n, rows, shard_stride_rows, k,
-        out_lse_mul, reinterpret_cast<__nv_bfloat16*>(out), out_lse);
-  }
-  return cudaGetLastError();
+  DependentLaunch dl(dim3((unsigned)blocks), dim3(kWarps * 32), stream);
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+  if (partials_fp32)
+    return cudaLaunchKernelEx(&dl.cfg, lse_combine_kernel<float>,
+                              static_cast<const float*>(partials), lses, n, rows,
+                              shard_stride_rows, k, out_lse_mul, o, out_lse);
+  return cudaLaunchKernelEx(&dl.cfg, lse_combine_kernel<__nv_bfloat16>,
+                            static_cast<const __nv_bfloat16*>(partials), lses, n, rows,
+                            shard_stride_rows, k, out_lse_mul, o, out_lse);
 }
 
 }  // namespace mla

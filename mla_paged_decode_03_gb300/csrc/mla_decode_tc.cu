@@ -1289,6 +1289,9 @@ __device__ __forceinline__ void combine_row(const Params& p, int b, int rt, int 
 __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   __shared__ int s_nt;
   __shared__ int2 s_m;
+  // launched as a dependent of the decode kernel: every block waits for it here, before any
+  // access to memory (so this grid also completes only after the decode kernel)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int u = blockIdx.x >> 4, rb = blockIdx.x & 15;      // 16 blocks of 8 rows per unit
   const int b = u / p.row_tiles, rt = u % p.row_tiles;
   if (threadIdx.x == 0) {
@@ -1546,8 +1549,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
     mla_decode_tc_kernel<false><<<2 * C, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_tc_combine_kernel<<<(unsigned)p.units * 16u, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  DependentLaunch dl(dim3((unsigned)p.units * 16u), dim3(256), stream);
+  return cudaLaunchKernelEx(&dl.cfg, mla_tc_combine_kernel, p);
 }
 
 }  // namespace mla
