@@ -300,6 +300,18 @@ def test_decode_grouped_schedule(B_, H_, q_len, lengths, cp, with_ws, kernel):
     _check_workload(w, with_workspace=with_ws)
 
 
+@pytest.mark.parametrize("with_ws,batched", [(True, True), (True, False), (False, True)])
+def test_decode_many_short_segments(with_ws, batched, kernel):
+    # 48 requests x 8 shards: many shard-requests with no key (1 or 2 positions over 8
+    # ranks), many of one partial tile, some long; each request's tiles are preceded on the
+    # split line by its start-up share, so group starts fall inside shares, inside tiles
+    # and on tile boundaries, and a group may hold nothing but shares
+    mix = [1, 2, 7, 63, 64, 65, 129, 640, 2000, 513, 8, 3000]
+    lengths = [mix[(7 * i) % len(mix)] for i in range(48)]
+    w = synth.make_custom(48, 128, 4, lengths, 64, 8, base_e=True, seed=4801)
+    _check_workload(w, relative=True, with_workspace=with_ws, batched=batched)
+
+
 def test_decode_block_table_with_wide_stride(kernel):
     w = synth.make_custom(2, 64, 2, [300, 129], 64, 2, seed=5, spare_columns=9)
     _check_workload(w)
