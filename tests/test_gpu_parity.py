@@ -123,6 +123,22 @@ def test_lse_merge_parity(n, fp32, base_e):
     assert torch.all(out[0, 0] == 0)
 
 
+@pytest.mark.parametrize("n,T,Hh", [(12, 7, 5), (33, 3, 3), (64, 1, 1), (9, 1, 3)])
+def test_lse_merge_few_rows_many_shards(n, T, Hh):
+    # few rows of many shards take several warps per row (each a strided subset of the
+    # shards, summed through shared memory): odd row counts, fewer rows than a block holds
+    g = torch.Generator().manual_seed(n * 13 + T)
+    parts = torch.randn(n, T, Hh, 512, generator=g).to(torch.bfloat16)
+    lses = torch.randn(n, T, Hh, generator=g) * 5 + 10
+    lses[torch.rand(n, T, Hh, generator=g) < 0.3] = float("-inf")
+    lses[:, -1, -1] = float("-inf")                       # a row with no shard at all
+    parts[:, -1, -1] = float("nan")                       # never read: every weight is 0
+    wo, wl = R.ref_lse_merge(H.f64(parts), H.f64(lses), True)
+    out, ol = M.lse_merge(parts.to(DEV), lses.to(DEV), out_lse=torch.empty(T, Hh, device=DEV))
+    H.compare(out, ol, wo, wl, what=f"merge n={n} rows={T * Hh}")
+    assert torch.all(out[-1, -1] == 0)
+
+
 def test_lse_merge_skips_nan_partials_of_empty_shards():
     parts = torch.randn(2, 4, 8, 512).to(torch.bfloat16)
     parts[1] = float("nan")
