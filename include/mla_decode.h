@@ -10,11 +10,17 @@
  *
  * Conventions shared by every call:
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.
- *     The library allocates no memory and keeps no state between calls other than one
- *     device status word per device (see mla_get_device_status).
+ *     The library allocates no memory when called.  Its device state is one status word
+ *     per device (see mla_get_device_status) and the fixed scratch array that
+ *     mla_decode_noalloc uses; its host state is per-device launch settings, filled on
+ *     a device's first call.
  *   - Every call is asynchronous on `stream` (the legacy default stream when NULL) and
  *     returns one of the MLA_* codes.  Argument errors are found on the host before
  *     anything is launched; mla_last_error() then returns a message (thread-local).
+ *   - Calls are stream-ordered: a call's kernels see every result issued before it on
+ *     the stream.  The split-KV combine of mla_decode and the kernel of lse_merge are
+ *     programmatic dependent launches: they may be scheduled while the kernel before
+ *     them drains, but wait for its completion before they read or write memory.
  *   - bf16 means IEEE bfloat16 stored as 16-bit words; results are rounded to nearest
  *     even.  Tensors are dense and row-major unless a stride is given.
  */
