@@ -8,7 +8,9 @@
 // 512, so every load and store of a warp covers 512 contiguous bytes (bf16) or 1 KB
 // (fp32).  The row max M of the n LSEs is reduced with warp shuffles; weights are
 // 2^(lse*k - M*k) with k = 1 (base-2 LSEs) or log2(e) (natural LSEs).  HBM-bound:
-// n * 1 KB (bf16) or n * 2 KB (fp32) read and 1 KB written per row.
+// n * 1 KB (bf16) or n * 2 KB (fp32) read and 1 KB written per row.  Few rows of many
+// bf16 shards take 2 or 4 warps per row instead (lse_combine_split_kernel), so that the
+// n rounds of loads of a row are spread over more warps.
 #include <math.h>
 
 #include <cuda_bf16.h>
