@@ -1286,6 +1286,30 @@ __device__ __forceinline__ void combine_row(const Params& p, int b, int rt, int 
     p.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * p.lse_mul : -INFINITY;
 }
 
+// unit_tiles in 32-bit arithmetic, for the combine's many blocks that only decide whether
+// their unit needs them: equal to it because lengths (causal_seqlens_global, seq_lens)
+// are below 2^31 and so is cp * interleave (both checked on the host).
+__device__ __forceinline__ int unit_tiles32(const Params& p, int u) {
+  const int b = u / p.row_tiles, rt = u % p.row_tiles;
+  const int last_row = min((rt + 1) * kM, p.rows) - 1;
+  const int sh = shard_of(p, b);
+  const int cap = seq_cap(p, b);
+  int keys = cap;
+  if (p.causal) {
+    const int g = __ldg(p.gseq + (b - sh * p.shard_B));
+    const int i = last_row / p.H;
+    const long long gi64 = (long long)g - (p.q_len - 1 - i);
+    const unsigned int gi = gi64 < 0 ? 0u : (unsigned int)gi64;
+    const unsigned int span = (unsigned int)p.span;
+    const unsigned int q = gi / span;
+    long long rem = (long long)(gi - q * span) - (long long)(p.rank + sh) * p.il;
+    rem = rem < 0 ? 0 : (rem > p.il ? p.il : rem);
+    const long long loc = (long long)q * p.il + rem;
+    keys = (int)(loc < cap ? loc : cap);
+  }
+  return (keys + kTile - 1) / kTile;
+}
+
 __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   __shared__ int s_nt;
   __shared__ int2 s_m;
@@ -1297,7 +1321,7 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(const Params p) {
   if (threadIdx.x == 0) {
     if (rt == 0 && rb == 0 && __ldg(p.seq_lens + b) > p.max_blocks * p.bs)
       atomicOr(p.status, MLA_STATUS_SEQ_TOO_LONG);
-    const int nt = unit_tiles(p, u);
+    const int nt = unit_tiles32(p, u);
     int2 m = make_int2(0, 0);
     if (nt > 0 && !p.whole_units) {
       m = p.meta[u];                          // first and last group holding the unit
