@@ -354,10 +354,10 @@ def time_e2e(step, steps, warmup, flush):
 # keyed by the SHA-256 of the tcgen05 kernel source they were taken on: a changed kernel
 # reports null until it is captured again.
 TRAFFIC = {
-    # spec, all 8 shards in one mla_decode_shards call: decode reads 2,984.2 MB and writes
+    # spec, all 8 shards in one mla_decode_shards call: decode reads 3,023.6 MB and writes
     # 131.8 MB, the split combine reads 19.0 MB (mean of 12 calls, one-pass capture of the
     # full workload)
-    ("spec", "45e04ba72522e352c829651ef58d69cf34583418d97371a32a3ebe489e27df39"): 3135013567,
+    ("spec", "fb4df4fe4dd00e46227fbd0fe766198c749aeeababc2759acef84367040f4fc5"): 3174349632,
 }
 
 
